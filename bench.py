@@ -1,0 +1,528 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV cache hot path on GB300.
+
+One step = one pass of the hot path over one synthetic batch:
+  decode workload (headline, Qwen3-0.6B-shaped: 16 q / 8 kv heads, head_dim
+  128, block_size 256, batch 64, context lengths U[512, 4096], 2048-block
+  pool): kv_build_decode_slots -> kv_store (one new token per sequence) ->
+  paged_attn_decode (split-K kernel + merge kernel).
+The headline value is the decode KV-read bandwidth of the whole step
+(sum_b ctx_b * Hkv * d * 2 bytes * 2 tensors / step time).  The prefill
+TFLOP/s (varlen and prefix-cache), the store_kvcache GB/s, and the large
+padded decode are measured in the same run and reported under "also".
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs an independent replica (the path has
+no exchange step); value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "paged-attn decode KV-read GB/s, prefill TFLOP/s, store_kvcache GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled with nvidia-smi while the GPU works
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        hi = [x for x in sm if x >= 0.5 * max(sm)]
+        return {"sm_mhz": statistics.median(hi), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return rank, world, local
+    if torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return 0, 1, 0
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# workloads on the device
+# ---------------------------------------------------------------------------
+def kv_bytes(ctx: torch.Tensor, heads) -> int:
+    return int(ctx.to(torch.int64).sum()) * heads.num_kv_heads * heads.head_dim * 2 * 2
+
+
+class DecodeStep:
+    """kv_build_decode_slots -> kv_store -> paged_attn_decode on resident inputs."""
+
+    def __init__(self, work, cache_seed: int):
+        from paged_kv_cache_303_gb300 import ops, workloads as W
+        self.ops, self.work, h = ops, work, work.heads
+        shape = (h.num_blocks, h.block_size, h.num_kv_heads, h.head_dim)
+        self.kc = W.fill_normal_(torch.empty(shape, dtype=torch.bfloat16, device="cuda"), cache_seed)
+        self.vc = W.fill_normal_(torch.empty(shape, dtype=torch.bfloat16, device="cuda"), cache_seed + 1)
+        self.q, self.k, self.v = (t.cuda() for t in (work.q, work.k, work.v))
+        self.bt = work.block_tables.cuda()
+        self.ctx = work.context_lens.cuda()
+        self.slots = torch.empty(work.batch, dtype=torch.int32, device="cuda")
+        self.out = torch.empty_like(self.q)
+        self.max_ctx = work.max_context_len
+        ws = ops.decode_workspace_size(work.batch, h.num_heads, h.num_kv_heads, h.head_dim, self.max_ctx)
+        self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device="cuda")
+        self.bytes = kv_bytes(work.context_lens, h)
+        live = int((work.context_lens > 0).sum())
+        self.qo_bytes = 2 * live * h.num_heads * h.head_dim * 2
+        self.store_bytes = live * h.num_kv_heads * h.head_dim * 2 * 4 + 4 * work.batch
+        self.launches = 4 if ws > 0 else 3
+
+    def attention(self):
+        h = self.work.heads
+        self.ops.paged_attn_decode(self.q, self.kc, self.vc, self.bt, self.ctx, self.max_ctx, h.scale,
+                                   out=self.out, workspace=self.ws)
+
+    def __call__(self, ev=None):
+        h = self.work.heads
+        self.ops.kv_build_decode_slots(self.bt, self.ctx, h.block_size, out=self.slots)
+        self.ops.kv_store(self.k, self.v, self.kc, self.vc, self.slots)
+        if ev is not None:
+            ev[0].record()
+        self.attention()
+        if ev is not None:
+            ev[1].record()
+
+
+class PrefillStep:
+    """kv_build_slot_mapping -> kv_store -> paged_attn_prefill on resident inputs."""
+
+    def __init__(self, work, cache_seed: int):
+        from paged_kv_cache_303_gb300 import ops, workloads as W
+        self.ops, self.work, h = ops, work, work.heads
+        shape = (h.num_blocks, h.block_size, h.num_kv_heads, h.head_dim)
+        self.kc = W.fill_normal_(torch.empty(shape, dtype=torch.bfloat16, device="cuda"), cache_seed)
+        self.vc = W.fill_normal_(torch.empty(shape, dtype=torch.bfloat16, device="cuda"), cache_seed + 1)
+        self.q, self.k, self.v = (t.cuda() for t in (work.q, work.k, work.v))
+        self.bt = work.block_tables.cuda()
+        self.start = work.prefix_lens.cuda()
+        self.cu_q, self.cu_k = work.cu_seqlens_q.cuda(), work.cu_seqlens_k.cuda()
+        self.slots = torch.empty(work.total_q, dtype=torch.int32, device="cuda")
+        self.out = torch.empty_like(self.q)
+        ws = ops.prefill_workspace_size(work.num_seqs, work.total_q, work.max_seqlen_q, h.num_heads)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device="cuda")
+        self.paged = work.has_prefix
+        self.flops = 4 * h.head_dim * h.num_heads * work.causal_pairs()
+        self.store_bytes = work.total_q * (h.num_kv_heads * h.head_dim * 2 * 4 + 4)
+        self.launches = 5
+
+    def store(self):
+        h = self.work.heads
+        self.ops.kv_store(self.k, self.v, self.kc, self.vc, self.slots)
+
+    def attention(self):
+        w, h = self.work, self.work.heads
+        if self.paged:
+            self.ops.paged_attn_prefill(self.q, None, None, self.cu_q, self.cu_k, w.max_seqlen_q,
+                                        w.max_seqlen_k, h.scale, k_cache=self.kc, v_cache=self.vc,
+                                        block_tables=self.bt, out=self.out, workspace=self.ws)
+        else:
+            self.ops.paged_attn_prefill(self.q, self.k, self.v, self.cu_q, self.cu_k, w.max_seqlen_q,
+                                        w.max_seqlen_k, h.scale, out=self.out, workspace=self.ws)
+
+    def __call__(self, ev=None, ev_store=None):
+        h = self.work.heads
+        self.ops.kv_build_slot_mapping(self.bt, self.start, self.cu_q, h.block_size, out=self.slots)
+        if ev_store is not None:
+            ev_store[0].record()
+        self.store()
+        if ev_store is not None:
+            ev_store[1].record()
+        if ev is not None:
+            ev[0].record()
+        self.attention()
+        if ev is not None:
+            ev[1].record()
+
+
+def time_steps(step, steps: int, warmup: int, world: int, kernel_events=True, store_events=False):
+    """Warm up, then time exactly `steps` steps between barriers/synchronizes.
+    Returns (total ms over ranks' max, mean attention-kernel ms, mean store ms)."""
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)] if kernel_events else None
+    sevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(steps)] if store_events else None
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(steps):
+        if store_events:
+            step(evs[i] if evs else None, sevs[i])
+        else:
+            step(evs[i] if evs else None)
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    total = max_over_ranks(start.elapsed_time(end), world)
+    kern = statistics.mean(a.elapsed_time(b) for a, b in evs) if evs else None
+    st = statistics.mean(a.elapsed_time(b) for a, b in sevs) if sevs else None
+    return total, kern, st
+
+
+# ---------------------------------------------------------------------------
+# end to end through the C ABI with host buffers
+# ---------------------------------------------------------------------------
+def e2e_decode(step: DecodeStep, steps: int, warmup: int, world: int):
+    """Every step copies its inputs (q, new k/v, context lengths, block tables)
+    from pinned host memory, runs the step through the public API, and reads
+    the output back to pinned host memory."""
+    w = step.work
+    host = {n: t.pin_memory() for n, t in (("q", w.q), ("k", w.k), ("v", w.v),
+                                           ("ctx", w.context_lens), ("bt", w.block_tables))}
+    dev = {"q": step.q, "k": step.k, "v": step.v, "ctx": step.ctx, "bt": step.bt}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for n, t in host.items():
+            dev[n].copy_(t, non_blocking=True)
+        step()
+        out_host.copy_(step.out, non_blocking=True)
+
+    total, _, _ = time_steps(lambda ev=None: one(), steps, warmup, world, kernel_events=False)
+    return total, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# the oracle as CPU baseline (bounded sample)
+# ---------------------------------------------------------------------------
+def cpu_baseline_decode(work, seconds: float = 10.0, max_rows: int = 64):
+    """The oracle (plain C, fp64, OpenMP over (row, head)) on the decode step:
+    decode slots, store and attention for the first `max_rows` rows, repeated
+    until about `seconds` of CPU work.  Returns (GB/s, cores, sample text)."""
+    import oracle
+    from paged_kv_cache_303_gb300 import workloads as W
+    h = work.heads
+    rows = list(range(min(max_rows, work.batch)))
+    lens = work.context_lens.numpy()[rows]
+    nblk = [(int(c) + h.block_size - 1) // h.block_size for c in lens]
+    # compact cache with just the blocks the sample reads, seeded history
+    g = W.generator(12345)
+    used = sum(nblk)
+    kc = W.normal_bf16((max(used, 1), h.block_size, h.num_kv_heads, h.head_dim), g, rmsnorm=False)
+    vc = W.normal_bf16((max(used, 1), h.block_size, h.num_kv_heads, h.head_dim), g, rmsnorm=False)
+    table = np.full((len(rows), max(nblk + [1])), -1, np.int32)
+    pos = 0
+    for i, n in enumerate(nblk):
+        table[i, :n] = np.arange(pos, pos + n)
+        pos += n
+    kb = kc.view(torch.int16).numpy().view(np.uint16)
+    vb = vc.view(torch.int16).numpy().view(np.uint16)
+    q = work.q[rows].contiguous().view(torch.int16).numpy().view(np.uint16)
+    k = work.k[rows].contiguous().view(torch.int16).numpy().view(np.uint16)
+    v = work.v[rows].contiguous().view(torch.int16).numpy().view(np.uint16)
+    cores = oracle.num_threads(0)
+    nbytes = int(lens.sum()) * h.num_kv_heads * h.head_dim * 4
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        slots = oracle.decode_slots(table, lens, h.block_size)
+        oracle.kv_store(k, v, kb, vb, slots)
+        oracle.decode(q, kb, vb, table, lens, h.scale, nthreads=0)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 1000:
+            break
+    gbs = nbytes * reps / el / 1e9
+    sample = (f"{len(rows)} of {work.batch} decode rows (contexts {int(lens.min())}-{int(lens.max())}),"
+              f" full step (slots, store, attention), {reps} repetitions in {el:.1f} s")
+    return gbs, cores, sample, el / reps
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world):
+    from paged_kv_cache_303_gb300 import build, ops, workloads as W
+    build.build()
+    pk, pk_kind = peaks()
+    hbm, tfl = float(pk["hbm_gbs"]), float(pk["bf16_tflops"])
+    dev_index = int(os.environ.get("LOCAL_RANK", "0"))
+
+    # headline: Qwen3-shaped decode step
+    dec = DecodeStep(W.qwen3_decode(), cache_seed=401)
+    for _ in range(3):
+        dec()
+    torch.cuda.synchronize()
+    # keep the clocks at load level, then sample them across the timed region
+    clocks = ClockSampler(dev_index).start() if rank == 0 else None
+    t_end = time.perf_counter() + 1.0
+    while time.perf_counter() < t_end:
+        for _ in range(50):
+            dec()
+        torch.cuda.synchronize()
+    total_ms, dec_ms, _ = time_steps(dec, args.steps, args.warmup, world)
+    clk = clocks.stop() if clocks else None
+    ms_per_step = total_ms / args.steps
+    value = dec.bytes * world * args.steps / (total_ms / 1e3) / 1e9
+    dec_achieved = (dec.bytes + dec.qo_bytes) / (dec_ms / 1e3) / 1e9
+
+    # end to end, host buffers
+    e2e_ms, h2d, d2h = e2e_decode(dec, args.steps, args.warmup, world)
+    e2e_val = dec.bytes * world * args.steps / (e2e_ms / 1e3) / 1e9
+    dec_bytes = dec.bytes
+    dec_launches = dec.launches
+    del dec
+    torch.cuda.empty_cache()
+
+    also = {}
+    # varlen prefill step (packed k/v), 8 prompts of U[128, 4096]
+    pre = PrefillStep(W.varlen_prefill(), cache_seed=501)
+    tot, pre_ms, st_ms = time_steps(pre, args.steps, args.warmup, world, store_events=True)
+    also["prefill_varlen"] = {
+        "workload": "varlen-prefill-8x: 8 prompts U[128,4096] (%d tokens), 16q/8kv/128d" % pre.work.total_q,
+        "tflops": round(pre.flops / (pre_ms / 1e3) / 1e12, 2),
+        "kernel_ms": round(pre_ms, 4), "step_ms": round(tot / args.steps, 4),
+        "roofline": {"bound": "tensor", "peak": tfl, "unit": "TFLOP/s",
+                     "frac": round(pre.flops / (pre_ms / 1e3) / 1e12 / tfl, 4)},
+        "flops_per_launch": pre.flops,
+    }
+    also["kv_store"] = {
+        "workload": "store of the varlen-prefill step's %d tokens (D=1024)" % pre.work.total_q,
+        "gbs": round(pre.store_bytes / (st_ms / 1e3) / 1e9, 1), "kernel_ms": round(st_ms, 4),
+        "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                     "frac": round(pre.store_bytes / (st_ms / 1e3) / 1e9 / hbm, 4)},
+        "bytes_per_launch": pre.store_bytes,
+    }
+    del pre
+    torch.cuda.empty_cache()
+    # prefix-cache prefill
+    pp = PrefillStep(W.prefix_prefill(), cache_seed=601)
+    tot, pp_ms, _ = time_steps(pp, args.steps, args.warmup, world)
+    also["prefill_prefix"] = {
+        "workload": "prefix-prefill-16x: prefix U{0..12}x256 + chunk U[64,1024] (%d new tokens)" % pp.work.total_q,
+        "tflops": round(pp.flops / (pp_ms / 1e3) / 1e12, 2), "kernel_ms": round(pp_ms, 4),
+        "roofline": {"bound": "tensor", "peak": tfl, "unit": "TFLOP/s",
+                     "frac": round(pp.flops / (pp_ms / 1e3) / 1e12 / tfl, 4)},
+    }
+    del pp
+    torch.cuda.empty_cache()
+    # large padded decode
+    if not args.skip_large:
+        big = DecodeStep(W.large_decode(), cache_seed=701)
+        tot, big_ms, _ = time_steps(big, args.steps, args.warmup, world)
+        also["decode_large"] = {
+            "workload": "large-decode-b256p32: 32q/8kv/128d, 256+32 pad rows, lognormal ctx [1k,32k],"
+                        " 40000-block pool",
+            "gbs": round(big.bytes / (big_ms / 1e3) / 1e9, 1), "kernel_ms": round(big_ms, 4),
+            "step_gbs": round(big.bytes / (tot / args.steps / 1e3) / 1e9, 1),
+            "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                         "frac": round(big.bytes / (big_ms / 1e3) / 1e9 / hbm, 4)},
+        }
+        del big
+        torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        gbs, cores, sample, _ = cpu_baseline_decode(W.qwen3_decode(), seconds=args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": sample}
+
+    traffic = None
+    prof = ROOT / "profiles" / "decode_traffic.json"
+    if prof.exists():
+        try:
+            traffic = json.loads(prof.read_text()).get("bytes_per_launch")
+        except ValueError:
+            traffic = None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "qwen3-decode-b64: 16q/8kv heads, head_dim 128, block_size 256, "
+                               "batch 64, ctx U[512,4096], 2048-block pool, seed 304",
+                   "step": "decode slots + kv_store + paged_attn_decode",
+                   "l2": "no flush: the %.2f GB KV read per step exceeds the 129 MB L2" % (dec_bytes / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4)},
+        "gpu_launches": dec_launches * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(dec_achieved, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(dec_achieved / hbm, 4), "traffic": traffic,
+                     "kernel": "paged_attn_decode (split kernel + merge kernel)",
+                     "kernel_ms": round(dec_ms, 4), "peak_source": f"{pk_kind} hbm_gbs"},
+        "cpu_baseline": cpu,
+        "clocks": clk,
+        "also": also,
+    }
+    return line
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is a bounded sample of the
+    same decode workload on the host cores."""
+    if rank != 0:
+        return None
+    from paged_kv_cache_303_gb300 import workloads as W
+    work = W.qwen3_decode()
+    per_step = []
+    cores, sample = None, None
+    for i in range(args.warmup + args.steps):
+        gbs, cores, sample, sec = cpu_baseline_decode(work, seconds=0.0, max_rows=8)
+        if i >= args.warmup:
+            per_step.append((gbs, sec))
+    secs = sum(s for _, s in per_step)
+    lens = work.context_lens.numpy()[:8]
+    nbytes = int(lens.sum()) * work.heads.num_kv_heads * work.heads.head_dim * 4
+    value = nbytes * len(per_step) / secs / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / len(per_step) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "qwen3-decode-b64 (first 8 of 64 rows per step)",
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": sample, "value": round(value, 4),
+                         "unit": "GB/s"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-large", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    rank, world, _ = dist_setup(args.gpus)
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged KV cache hot path.
+ *
+ * The operations follow the attention layer of the nano-vllm engine as the
+ * pages describe it:
+ *   - "L17: Qwen3 attention sub-layer" (nano-vllm series), §3 (GQA), §5.1
+ *     (store_kvcache), §5.2 (FlashAttention / online softmax), §5.3 (the
+ *     prefill, prefix-cache and decode calls), §7 (integration check);
+ *   - "Lesson 04: where exactly does the KV go", §1 (the five forward
+ *     inputs), §2 (slot_mapping), §3 (the write kernel), §4 (two
+ *     FlashAttention calls), §9 (decode slot).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *    library never allocates, frees or keeps a pointer past the call.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and never synchronises, except in validate mode
+ *    (pkv_set_validate), which synchronises the stream after the launch and
+ *    reports device-side checks.
+ *  - bf16 tensors are passed as pkv_bf16 (the raw 16-bit pattern).
+ *  - Strides are in ELEMENTS.  "Row" means one token (or one decode
+ *    sequence).  Inside a row, heads are contiguous and each head's head_dim
+ *    elements are contiguous (head stride == head_dim, element stride 1), as
+ *    store_kvcache asserts in §5.1; the row stride itself is free (k and v
+ *    may be views of a fused qkv projection output, §3).
+ *  - The cache of one layer is two tensors k_cache, v_cache, each
+ *    [num_blocks, block_size, num_kv_heads, head_dim] contiguous bf16; slot
+ *    s = block_id * block_size + offset addresses the num_kv_heads*head_dim
+ *    elements at s * num_kv_heads * head_dim (Lesson 04, §2).
+ *  - block_tables is [num_seqs, bt_stride] int32; row i lists the physical
+ *    blocks of sequence i in logical order, padded with -1 (Lesson 04, §1).
+ *    max_blocks_per_seq <= bt_stride is the number of usable columns.
+ *  - Query head h uses kv head h / (num_heads / num_kv_heads) (§3).
+ *  - Return value: PKV_OK or a PKV_ERR_* code; pkv_last_error() describes the
+ *    last failure on the calling host thread.  Invalid arguments are
+ *    rejected before anything is launched.  Data-dependent problems that
+ *    only the device can see (a slot or block id out of range, a -1 inside
+ *    the used part of a block table, a length above the stated maximum) never
+ *    cause an out-of-bounds access: the offending row/token is skipped or
+ *    clamped and a sticky bit is set in the device status word
+ *    (pkv_device_status).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pkv_bf16;                 /* raw bf16 bits */
+typedef struct CUstream_st *pkv_stream_t;  /* same type as cudaStream_t */
+
+enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shapes */
+    PKV_ERR_UNSUPPORTED = 2,   /* a valid request this build does not handle (e.g. head_dim) */
+    PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than the *_workspace_size() */
+    PKV_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed */
+    PKV_ERR_DEVICE_CHECK = 5,  /* validate mode: the device flagged invalid data */
+    PKV_ERR_DEVICE_TIMEOUT = 6 /* validate mode: a bounded device wait gave up */
+};
+
+/* device status bits (sticky until cleared) */
+enum {
+    PKV_STATUS_BAD_SLOT = 1u << 0,    /* kv_store: slot < -1 or >= num_slots        */
+    PKV_STATUS_BAD_BLOCK = 1u << 1,   /* block table entry < 0 or >= num_blocks     */
+    PKV_STATUS_BAD_LENGTH = 1u << 2,  /* length above its declared maximum / table   */
+    PKV_STATUS_TIMEOUT = 1u << 3      /* a bounded wait on an mbarrier expired        */
+};
+
+/* Message describing the last error returned on this host thread ("" if none). */
+const char *pkv_last_error(void);
+
+/* ABI version (increments on any signature change). */
+int pkv_version(void);
+
+/* Validate mode: when on, every entry point synchronises `stream` after its
+ * launches and turns a non-zero device status into PKV_ERR_DEVICE_CHECK or
+ * PKV_ERR_DEVICE_TIMEOUT (clearing it).  Off by default; the environment
+ * variable PKV_VALIDATE=1 turns it on at load time. */
+void pkv_set_validate(int on);
+
+/* Synchronise `stream`, then OR together the status words of every kernel
+ * family of the current device into *status; clear them when `clear` != 0. */
+int pkv_device_status(pkv_stream_t stream, uint32_t *status, int clear);
+
+/* ------------------------------------------------------------------------
+ * kv_build_slot_mapping -- Lesson 04, §2 (and §7, Exercise A).
+ *
+ * For sequence i with start[i] tokens already cached and
+ * cu_seqlens_q[i+1] - cu_seqlens_q[i] new tokens, token t of the step
+ * (logical position p = start[i] + t) is assigned
+ *     slot_mapping[cu_seqlens_q[i] + t] = block_tables[i][p / block_size] * block_size
+ *                                         + p % block_size.
+ * The first block may start mid-block (chunked prefill), the last may end
+ * mid-block.
+ *   block_tables  [num_seqs, bt_stride] int32 (device)
+ *   start         [num_seqs] int32 (device), cached tokens per sequence
+ *   cu_seqlens_q  [num_seqs+1] int32 (device), prefix sums of new tokens
+ *   slot_mapping  [num_tokens] int32 (device, output); num_tokens is the
+ *                 capacity, cu_seqlens_q[num_seqs] must not exceed it.
+ * A table entry that is missing (-1 or beyond max_blocks_per_seq) yields
+ * slot -1 and sets PKV_STATUS_BAD_BLOCK.
+ * ---------------------------------------------------------------------- */
+int kv_build_slot_mapping(const int32_t *block_tables, int64_t bt_stride,
+                          int32_t max_blocks_per_seq, const int32_t *start,
+                          const int32_t *cu_seqlens_q, int32_t num_seqs,
+                          int32_t block_size, int32_t *slot_mapping,
+                          int32_t num_tokens, pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * kv_build_decode_slots -- Lesson 04, §9 item 1; L17 §7.
+ *
+ * One new token per row: with context_lens[b] counting that token,
+ *     slot_mapping[b] = block_tables[b][(ctx-1) / block_size] * block_size
+ *                       + (ctx-1) % block_size
+ * (the page's block_table[-1] * block_size + last_block_num_tokens - 1).
+ * context_lens[b] == 0 marks a padding row of a CUDA-graph batch (L17,
+ * §5.1) and yields slot -1.
+ * ---------------------------------------------------------------------- */
+int kv_build_decode_slots(const int32_t *block_tables, int64_t bt_stride,
+                          int32_t max_blocks_per_seq, const int32_t *context_lens,
+                          int32_t batch, int32_t block_size, int32_t *slot_mapping,
+                          pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * kv_store -- L17 §5.1 (store_kvcache), Lesson 04 §3.
+ *
+ * For every token n in [0, num_tokens) whose slot s = slot_mapping[n] is not
+ * -1, copy the D = num_kv_heads * head_dim elements of key row n into
+ * k_cache[s*D .. s*D+D) and of value row n into v_cache likewise.  A -1 slot
+ * (a padding token) leaves the cache untouched.  Bit-exact copy.
+ *   key, value  [num_tokens, num_kv_heads, head_dim] bf16, row strides
+ *               key_row_stride / value_row_stride (>= D)
+ *   k_cache, v_cache  num_slots * D bf16 each
+ *   slot_mapping [num_tokens] int32
+ * Two tokens with the same slot in one call race (invalid input).  A slot
+ * outside [-1, num_slots) is skipped and sets PKV_STATUS_BAD_SLOT.
+ * ---------------------------------------------------------------------- */
+int kv_store(const pkv_bf16 *key, int64_t key_row_stride,
+             const pkv_bf16 *value, int64_t value_row_stride,
+             pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+             const int32_t *slot_mapping, int32_t num_tokens,
+             int32_t num_kv_heads, int32_t head_dim, int64_t num_slots,
+             pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * paged_attn_prefill -- L17 §5.2/§5.3 (flash_attn_varlen_func with
+ * causal=True), Lesson 04 §4.
+ *
+ * Varlen causal attention over packed sequences.  Sequence i owns query rows
+ * [cu_seqlens_q[i], cu_seqlens_q[i+1]) (Lq_i rows) and Lk_i =
+ * cu_seqlens_k[i+1] - cu_seqlens_k[i] >= Lq_i keys.  Query row t of the
+ * sequence (0 <= t < Lq_i) attends to keys j <= Lk_i - Lq_i + t (causal mask
+ * aligned to the last key: the cached prefix is seen by every new token):
+ *     out[row, h] = sum_j softmax_j(softmax_scale * q[row,h] . k_j) v_j
+ *     lse[row, h] = log sum_j exp(softmax_scale * q[row,h] . k_j)
+ * Keys and values come from
+ *   - the packed k, v [total_k, num_kv_heads, head_dim] when
+ *     block_tables == NULL (plain prefill; key j of sequence i is row
+ *     cu_seqlens_k[i] + j), or
+ *   - the paged caches when block_tables != NULL (prefix-cache hit, §5.3:
+ *     the prefix plus the chunk that kv_store has just written; key j lives
+ *     at slot block_tables[i][j / block_size] * block_size + j % block_size).
+ *   q    [total_q, num_heads, head_dim] bf16, row stride q_row_stride
+ *   out  [total_q, num_heads, head_dim] bf16, row stride out_row_stride
+ *   lse  [total_q, num_heads] fp32 or NULL
+ * Supported: head_dim 128 (and 64), num_heads % num_kv_heads == 0; row
+ * strides multiples of 8 elements, pointers 16-byte aligned.
+ * workspace: device scratch of at least paged_attn_prefill_workspace_size()
+ * bytes (may be NULL when that is 0); its content need not be initialised.
+ * ---------------------------------------------------------------------- */
+int paged_attn_prefill(const pkv_bf16 *q, int64_t q_row_stride,
+                       const pkv_bf16 *k, int64_t k_row_stride,
+                       const pkv_bf16 *v, int64_t v_row_stride,
+                       const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, int64_t num_blocks,
+                       const int32_t *block_tables, int64_t bt_stride, int32_t max_blocks_per_seq,
+                       const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                       int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_seqs,
+                       int32_t total_q, int32_t total_k,
+                       int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t block_size, float softmax_scale,
+                       pkv_bf16 *out, int64_t out_row_stride, float *lse,
+                       void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+size_t paged_attn_prefill_workspace_size(int32_t num_seqs, int32_t total_q,
+                                         int32_t max_seqlen_q, int32_t num_heads);
+
+/* ------------------------------------------------------------------------
+ * paged_attn_decode -- L17 §5.3 (flash_attn_with_kvcache), Lesson 04 §4.
+ *
+ * One query per sequence: row b attends to the context_lens[b] tokens of its
+ * paged cache, the token kv_store wrote this step included (§4: the write
+ * comes first, so step t sees position t):
+ *     out[b, h] = sum_{j < ctx_b} softmax_j(softmax_scale * q[b,h] . k_j) v_j
+ * with k_j at slot block_tables[b][j / block_size] * block_size + j % block_size.
+ * A row with context_len 0 (padding) gets out = 0 and lse = -inf.
+ * The keys of a (row, kv head) are split into chunks processed in parallel
+ * and merged with the online-softmax rescaling of §5.2.
+ *   q    [batch, num_heads, head_dim] bf16, row stride q_row_stride
+ *   out  [batch, num_heads, head_dim] bf16, row stride out_row_stride
+ *   lse  [batch, num_heads] fp32 or NULL
+ *   max_context_len >= every context_lens[b] (host-side bound used to size
+ *   the launch; a larger device value is clamped and flagged).
+ * workspace: at least paged_attn_decode_workspace_size() bytes of device
+ * scratch (NULL when that is 0); content need not be initialised.  Calls
+ * that share a workspace must be ordered on the device.
+ * Supported: head_dim 64 or 128; num_heads / num_kv_heads in {1,2,4,8}.
+ * ---------------------------------------------------------------------- */
+int paged_attn_decode(const pkv_bf16 *q, int64_t q_row_stride,
+                      const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, int64_t num_blocks,
+                      const int32_t *block_tables, int64_t bt_stride, int32_t max_blocks_per_seq,
+                      const int32_t *context_lens, int32_t batch,
+                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t max_context_len, float softmax_scale,
+                      pkv_bf16 *out, int64_t out_row_stride, float *lse,
+                      void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+size_t paged_attn_decode_workspace_size(int32_t batch, int32_t num_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t max_context_len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

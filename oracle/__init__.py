@@ -90,6 +90,9 @@ def _load():
             "orc_decode": ([_P, _I64, _P, _P, _I64, _P, _I64, _I32, _P, _I32,
                             _I32, _I32, _I32, _I32, _D, _P, _P, _INT], _INT),
             "orc_online_softmax": ([_P, _P, _I64, _I64, _I64, _P, _P, _P, _P], _INT),
+            "orc_prefill_rows": ([_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _I32,
+                                  _P, _P, _I32, _I32, _I32, _I32, _I32, _D, _P, _I64, _P, _P,
+                                  _INT], _INT),
             "orc_decode_split": ([_P, _I64, _P, _P, _I64, _P, _I64, _I32, _P, _I32,
                                   _I32, _I32, _I32, _I32, _D, _I64, _P, _P], _INT),
         }
@@ -231,6 +234,35 @@ def prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, scale, *, k_cache=None, v_cache
                                  len(cu_q) - 1, hq, hkv, d, bs, float(scale), _ptr(out),
                                  _ptr(lse), nthreads)
     _check(rc, "prefill")
+    return out, lse
+
+
+def prefill_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, scale, rows, *, k_cache=None,
+                 v_cache=None, block_tables=None, nthreads=0):
+    """prefill() restricted to the given global query rows; returns
+    (out fp64 [len(rows), Hq, d], lse fp64 [len(rows), Hq])."""
+    q, q_rs = _rows(q)
+    nq, hq, d = q.shape
+    cu_q, cu_k = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.zeros((len(rows), hq, d), dtype=np.float64)
+    lse = np.zeros((len(rows), hq), dtype=np.float64)
+    if block_tables is None:
+        k, k_rs = _rows(k)
+        v, v_rs = _rows(v)
+        rc = _load().orc_prefill_rows(_ptr(q), q_rs, _ptr(k), k_rs, _ptr(v), v_rs, None, None, 0,
+                                      None, 0, 0, _ptr(cu_q), _ptr(cu_k), len(cu_q) - 1, hq,
+                                      k.shape[1], d, 1, float(scale), _ptr(rows), len(rows),
+                                      _ptr(out), _ptr(lse), nthreads)
+    else:
+        k_cache, v_cache = _u16(k_cache), _u16(v_cache)
+        nb, bs, hkv, _ = k_cache.shape
+        bt, stride, width = _table(block_tables)
+        rc = _load().orc_prefill_rows(_ptr(q), q_rs, None, 0, None, 0, _ptr(k_cache),
+                                      _ptr(v_cache), nb, _ptr(bt), stride, width, _ptr(cu_q),
+                                      _ptr(cu_k), len(cu_q) - 1, hq, hkv, d, bs, float(scale),
+                                      _ptr(rows), len(rows), _ptr(out), _ptr(lse), nthreads)
+    _check(rc, "prefill_rows")
     return out, lse
 
 

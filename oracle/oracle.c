@@ -641,3 +641,78 @@ int orc_decode_split(const uint16_t *q, int64_t q_rs,
     free(sm); free(sl); free(sacc); free(s);
     return rc;
 }
+
+/* Prefill restricted to selected query rows (global row indices into q),
+ * for checking full-size launches on a sample: rows[r] is looked up in
+ * cu_seqlens_q, then computed exactly as orc_prefill computes it.
+ * out is [n_rows, Hq, d], lse [n_rows, Hq] (optional). */
+int orc_prefill_rows(const uint16_t *q, int64_t q_rs,
+                     const uint16_t *k, int64_t k_rs, const uint16_t *v, int64_t v_rs,
+                     const uint16_t *k_cache, const uint16_t *v_cache, int64_t num_blocks,
+                     const int32_t *block_tables, int64_t bt_stride, int32_t max_blocks,
+                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                     int32_t num_seqs, int32_t Hq, int32_t Hkv, int32_t d,
+                     int32_t block_size, double scale, const int64_t *rows, int64_t n_rows,
+                     double *out, double *lse, int nthreads)
+{
+    if (check_heads(Hq, Hkv, d) || num_seqs < 0 || n_rows < 0)
+        return ORC_EARG;
+    if (block_tables && (block_size <= 0 || !k_cache || !v_cache))
+        return ORC_EARG;
+    if (!block_tables && (!k || !v))
+        return ORC_EARG;
+    orc_attn_args a = {q, q_rs, k, k_rs, v, v_rs, k_cache, v_cache, num_blocks,
+                       block_tables, bt_stride, max_blocks, Hq, Hkv, d, block_size, scale};
+    int64_t max_lk = 1;
+    for (int32_t i = 0; i < num_seqs; ++i) {
+        int64_t lq = (int64_t)cu_seqlens_q[i + 1] - cu_seqlens_q[i];
+        int64_t lk = (int64_t)cu_seqlens_k[i + 1] - cu_seqlens_k[i];
+        if (lq < 0 || lk < lq)
+            return ORC_ELEN;
+        if (lk > max_lk)
+            max_lk = lk;
+    }
+    int rc = ORC_OK;
+    set_threads(nthreads);
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)max_lk);
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!s || !o) {
+#pragma omp atomic write
+            rc = ORC_ENOMEM;
+        }
+#pragma omp for collapse(2) schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            for (int32_t h = 0; h < Hq; ++h) {
+                if (!s || !o)
+                    continue;
+                int64_t row = rows[r];
+                int32_t i = 0;
+                while (i < num_seqs && cu_seqlens_q[i + 1] <= row)
+                    ++i;
+                if (i >= num_seqs || row < cu_seqlens_q[i]) {
+#pragma omp atomic write
+                    rc = ORC_EARG;
+                    continue;
+                }
+                int64_t lq = (int64_t)cu_seqlens_q[i + 1] - cu_seqlens_q[i];
+                int64_t lk = (int64_t)cu_seqlens_k[i + 1] - cu_seqlens_k[i];
+                int64_t t = row - cu_seqlens_q[i];
+                double l;
+                int e = attend_row(&a, i, cu_seqlens_k[i], row, h, lk - lq + t + 1, s, o, &l);
+                if (e) {
+#pragma omp atomic write
+                    rc = e;
+                    continue;
+                }
+                memcpy(out + (r * Hq + h) * (int64_t)d, o, sizeof(double) * (size_t)d);
+                if (lse)
+                    lse[r * Hq + h] = l;
+            }
+        }
+        free(s);
+        free(o);
+    }
+    return rc;
+}

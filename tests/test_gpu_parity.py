@@ -1,0 +1,521 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact for slot mapping and the cache scatter; for attention every output
+element must satisfy |gpu - oracle| <= 1e-2 + 1e-2 * |oracle| (bf16 inputs,
+fp32 accumulation on the GPU, fp64 in the oracle, bf16 output).  Inputs are
+the seeded workloads; the oracle never sees a value the CUDA path produced:
+each side builds its own slot mapping and its own cache from the same inputs.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_303_gb300 import ops
+from paged_kv_cache_303_gb300 import workloads as W
+from _util import bits, bf16_bits_of, f64, from_bits, golden
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+NAN_BITS = 0x7FC1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_303_gb300 import build
+    build.build()
+    ops.device_status(clear=True)
+    yield
+    assert ops.device_status(clear=True) == 0, "a kernel flagged its input"
+
+
+def dev(t):
+    return t.to("cuda")
+
+
+def assert_close(gpu: torch.Tensor, ref: np.ndarray, what: str, tol=TOL):
+    g = gpu.detach().float().cpu().double().numpy()
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    err = np.abs(g - ref)
+    bound = tol + tol * np.abs(ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)[:5].tolist()
+        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside tolerance, "
+                             f"max abs {np.nanmax(err):.3e}, first bad {idx}")
+
+
+# ---------------------------------------------------------------------------
+# slot mapping (bit-exact)
+# ---------------------------------------------------------------------------
+def test_slot_mapping_exercise():
+    g = golden("t3_slot_mapping.json")
+    bt = dev(torch.tensor([g["block_table"]], dtype=torch.int32))
+    for case in g["cases"]:
+        start = dev(torch.tensor([case["cached"]], dtype=torch.int32))
+        cu = dev(torch.tensor([0, case["new_tokens"]], dtype=torch.int32))
+        got = ops.kv_build_slot_mapping(bt, start, cu, g["block_size"])
+        assert got.cpu().tolist() == case["slot_mapping"]
+
+
+@pytest.mark.parametrize("bs", [1, 4, 16, 256])
+def test_slot_mapping_random(bs):
+    rng = np.random.default_rng(100 + bs)
+    for _ in range(10):
+        n = int(rng.integers(1, 40))
+        start = rng.integers(0, 4 * bs + 3, n).astype(np.int32)
+        lens = rng.integers(0, 4 * bs + 3, n).astype(np.int32)
+        width = int(((start + lens + bs - 1) // bs).max()) + 2
+        bt = rng.permutation(n * width * 2)[: n * width].reshape(n, width).astype(np.int32)
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        ref = oracle.slot_mapping(bt, start, cu, bs)
+        got = ops.kv_build_slot_mapping(dev(torch.from_numpy(bt)), dev(torch.from_numpy(start)),
+                                        dev(torch.from_numpy(cu)), bs)
+        assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def test_decode_slots_with_padding():
+    work = W.large_decode(batch=40, pads=8, num_blocks=8000)
+    ref = oracle.decode_slots(work.block_tables, work.context_lens, work.heads.block_size)
+    got = ops.kv_build_decode_slots(dev(work.block_tables), dev(work.context_lens),
+                                    work.heads.block_size)
+    assert np.array_equal(got.cpu().numpy(), ref)
+    assert (ref[-8:] == -1).all()
+
+
+def test_missing_table_entry_is_flagged_not_written():
+    bt = dev(torch.tensor([[3, -1]], dtype=torch.int32))
+    got = ops.kv_build_slot_mapping(bt, dev(torch.tensor([0], dtype=torch.int32)),
+                                    dev(torch.tensor([0, 6], dtype=torch.int32)), 4)
+    assert got.cpu().tolist() == [12, 13, 14, 15, -1, -1]
+    assert ops.device_status(clear=True) & ops.PKV_STATUS_BAD_BLOCK
+
+
+# ---------------------------------------------------------------------------
+# kv_store (bit-exact)
+# ---------------------------------------------------------------------------
+def test_store_scatter_toy():
+    g = golden("t1_scatter_toy.json")
+    src = from_bits(bf16_bits_of(g["src"]).reshape(3, 1, 4))
+    kc = torch.zeros(3, 1, 1, 4, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    ops.kv_store(dev(src), dev(src), kc, vc, dev(torch.tensor(g["slot"], dtype=torch.int32)))
+    assert np.array_equal(kc.view(3, 4).float().cpu().numpy(), np.array(g["dst"], np.float32))
+
+
+def test_store_kvcache_example_with_skip():
+    g = golden("t2_store_kvcache.json")
+    key = from_bits(bf16_bits_of(g["key"]))
+    value = from_bits(bf16_bits_of(np.array(g["key"]) + g["value_offset"]))
+    kc = torch.full((1, 4, 2, 2), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full((1, 4, 2, 2), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ops.kv_store(dev(key), dev(value), kc, vc, dev(torch.tensor(g["slot_mapping"], dtype=torch.int32)))
+    rows = kc.view(4, 4).float().cpu().numpy()
+    assert np.array_equal(rows[:3], np.array(g["k_cache_rows"][:3], np.float32))
+    assert np.isnan(rows[3]).all()                       # no token maps to slot 3
+    assert np.array_equal(vc.view(4, 4)[0].float().cpu().numpy(),
+                          np.array(g["v_cache_slot0"], np.float32))
+
+
+@pytest.mark.parametrize("fused,hkv,d", [(False, 8, 128), (True, 8, 128), (False, 2, 64),
+                                         (True, 3, 20)])
+def test_store_random_vs_oracle(fused, hkv, d):
+    heads = W.Heads(2 * hkv, hkv, d, 16, 64)
+    rng = np.random.default_rng(7)
+    n = 300
+    work = W.prefill_work(heads, [n], seed=200)
+    if fused:   # k/v as views of one fused projection output (row stride > Hkv*d)
+        qkv = torch.cat([work.q.flatten(1), work.k.flatten(1), work.v.flatten(1)], 1)
+        qw = heads.num_heads * d
+        key = qkv[:, qw:qw + hkv * d].view(n, hkv, d)
+        value = qkv[:, qw + hkv * d:].view(n, hkv, d)
+    else:
+        key, value = work.k, work.v
+    slots = rng.permutation(heads.num_blocks * heads.block_size)[:n].astype(np.int32)
+    slots[rng.random(n) < 0.1] = -1
+    kc, vc = W.history_cache(heads, 201)
+    kref, vref = bits(kc).copy(), bits(vc).copy()
+    oracle.kv_store(bits(key), bits(value), kref, vref, slots)
+    gk, gv = dev(kc), dev(vc)
+    if fused:
+        dq = dev(qkv)
+        dkey = dq[:, qw:qw + hkv * d].view(n, hkv, d)
+        dval = dq[:, qw + hkv * d:].view(n, hkv, d)
+    else:
+        dkey, dval = dev(key), dev(value)
+    ops.kv_store(dkey, dval, gk, gv, dev(torch.from_numpy(slots)))
+    assert np.array_equal(bits(gk), kref) and np.array_equal(bits(gv), vref)
+
+
+def test_store_bad_slot_is_skipped_and_flagged():
+    kc = torch.zeros(2, 4, 1, 8, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    x = torch.ones(3, 1, 8, dtype=torch.bfloat16, device="cuda")
+    ops.kv_store(x, x, kc, vc, dev(torch.tensor([1, 8, -5], dtype=torch.int32)))
+    assert ops.device_status(clear=True) & ops.PKV_STATUS_BAD_SLOT
+    assert kc.view(8, 8)[1].eq(1).all() and kc.view(8, 8)[[0, 2, 3, 4, 5, 6, 7]].eq(0).all()
+
+
+# ---------------------------------------------------------------------------
+# decode
+# ---------------------------------------------------------------------------
+def _poison_unused(kc: torch.Tensor, vc: torch.Tensor, block_tables, lens):
+    """NaN every cache slot that no row reads (positions >= its length)."""
+    nb, bs = kc.shape[0], kc.shape[1]
+    used = torch.zeros(nb * bs, dtype=torch.bool)
+    for row, n in zip(block_tables.tolist(), lens.tolist()):
+        for j in range(int(n)):
+            used[row[j // bs] * bs + j % bs] = True
+    flat_k, flat_v = kc.view(nb * bs, -1), vc.view(nb * bs, -1)
+    flat_k[~used] = float("nan")
+    flat_v[~used] = float("nan")
+
+
+def _decode_case(heads, ctx, seed, poison=True, lse=True):
+    work = W.decode_work(heads, ctx, seed=seed)
+    kc, vc = W.history_cache(heads, seed + 1)
+    if poison:
+        _poison_unused(kc, vc, work.block_tables, work.context_lens)
+    # oracle side: write the new token with its own slot mapping, then decode
+    kref, vref = bits(kc).copy(), bits(vc).copy()
+    slots = oracle.decode_slots(work.block_tables, work.context_lens, heads.block_size)
+    oracle.kv_store(bits(work.k), bits(work.v), kref, vref, slots)
+    ref, ref_lse = oracle.decode(bits(work.q), kref, vref, work.block_tables, work.context_lens,
+                                 heads.scale, nthreads=0)
+    # GPU side through the C ABI
+    gk, gv = dev(kc), dev(vc)
+    bt, ctxd = dev(work.block_tables), dev(work.context_lens)
+    gslots = ops.kv_build_decode_slots(bt, ctxd, heads.block_size)
+    ops.kv_store(dev(work.k), dev(work.v), gk, gv, gslots)
+    out, out_lse = ops.paged_attn_decode(dev(work.q), gk, gv, bt, ctxd, max(1, work.max_context_len),
+                                         heads.scale, return_lse=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(gslots.cpu().numpy(), slots)
+    assert_close(out, ref, "decode out")
+    fin = np.isfinite(ref_lse)
+    got_lse = out_lse.cpu().double().numpy()
+    assert np.array_equal(np.isfinite(got_lse), fin)
+    if lse:
+        assert np.allclose(got_lse[fin], ref_lse[fin], atol=2e-3, rtol=1e-4)
+    return work
+
+
+DECODE_SHAPES = [
+    # Hq, Hkv, d, bs, contexts
+    (16, 8, 128, 256, [1, 63, 64, 65, 255, 256, 257, 1000, 2047]),
+    (4, 2, 64, 4, [7, 4, 1, 13, 64, 100]),
+    (32, 8, 128, 256, [1500, 0, 3000, 0, 129]),
+    (8, 8, 128, 16, [33, 200, 511]),
+    (16, 2, 128, 64, [65, 640, 1]),
+    (8, 1, 64, 32, [300, 31, 32]),
+]
+
+
+@pytest.mark.parametrize("shape", DECODE_SHAPES, ids=lambda s: f"{s[0]}q{s[1]}kv{s[2]}d_bs{s[3]}")
+@pytest.mark.parametrize("chunk_tiles", [None, "1", "3"])
+def test_decode_vs_oracle(shape, chunk_tiles, monkeypatch):
+    hq, hkv, d, bs, ctx = shape
+    if chunk_tiles:
+        monkeypatch.setenv("PKV_DECODE_CHUNK_TILES", chunk_tiles)
+    need = sum((c + bs - 1) // bs for c in ctx) + 3
+    heads = W.Heads(hq, hkv, d, bs, need)
+    _decode_case(heads, ctx, seed=300 + hq + d + bs)
+
+
+def test_decode_tiny_pipeline():
+    """Config 'tiny': slot mapping + store of the two prompts, then one decode
+    step per sequence (new tokens at positions 6 and 3)."""
+    pre, dec = W.tiny()
+    h = pre.heads
+    kc, vc = W.empty_cache(h)
+    kref, vref = bits(kc).copy(), bits(vc).copy()
+    slots = oracle.slot_mapping(pre.block_tables, pre.prefix_lens, pre.cu_seqlens_q, h.block_size)
+    oracle.kv_store(bits(pre.k), bits(pre.v), kref, vref, slots)
+    dslots = oracle.decode_slots(dec.block_tables, dec.context_lens, h.block_size)
+    assert dslots[0] == 38
+    oracle.kv_store(bits(dec.k), bits(dec.v), kref, vref, dslots)
+    ref, _ = oracle.decode(bits(dec.q), kref, vref, dec.block_tables, dec.context_lens, h.scale)
+    ref_pre, _ = oracle.prefill(bits(pre.q), bits(pre.k), bits(pre.v), pre.cu_seqlens_q,
+                                pre.cu_seqlens_k, h.scale)
+
+    gk, gv = dev(kc), dev(vc)
+    bt = dev(pre.block_tables)
+    gs = ops.kv_build_slot_mapping(bt, dev(pre.prefix_lens), dev(pre.cu_seqlens_q), h.block_size)
+    ops.kv_store(dev(pre.k), dev(pre.v), gk, gv, gs)
+    out_pre = ops.paged_attn_prefill(dev(pre.q), dev(pre.k), dev(pre.v), dev(pre.cu_seqlens_q),
+                                     dev(pre.cu_seqlens_k), pre.max_seqlen_q, pre.max_seqlen_k, h.scale)
+    gds = ops.kv_build_decode_slots(bt, dev(dec.context_lens), h.block_size)
+    ops.kv_store(dev(dec.k), dev(dec.v), gk, gv, gds)
+    out = ops.paged_attn_decode(dev(dec.q), gk, gv, bt, dev(dec.context_lens), 7, h.scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(gs.cpu().numpy(), slots)
+    assert np.array_equal(bits(gk), kref) and np.array_equal(bits(gv), vref)
+    assert_close(out_pre, ref_pre, "tiny prefill")
+    assert_close(out, ref, "tiny decode")
+
+
+def test_decode_qwen3_full_size():
+    """Qwen3-shaped decode, batch 64, contexts U[512, 4096]: every output."""
+    work = W.qwen3_decode()
+    h = work.heads
+    kc, vc = W.history_cache(h, 401)
+    kref, vref = bits(kc).copy(), bits(vc).copy()
+    slots = oracle.decode_slots(work.block_tables, work.context_lens, h.block_size)
+    oracle.kv_store(bits(work.k), bits(work.v), kref, vref, slots)
+    ref, _ = oracle.decode(bits(work.q), kref, vref, work.block_tables, work.context_lens, h.scale)
+    gk, gv = dev(kc), dev(vc)
+    bt, ctx = dev(work.block_tables), dev(work.context_lens)
+    ops.kv_store(dev(work.k), dev(work.v), gk, gv, ops.kv_build_decode_slots(bt, ctx, h.block_size))
+    out = ops.paged_attn_decode(dev(work.q), gk, gv, bt, ctx, work.max_context_len, h.scale)
+    assert_close(out, ref, "qwen3 decode")
+
+
+def _compact_blocks(block_tables, rows, lens):
+    """For sampled rows, the physical blocks they read and a table remapped to
+    a compact cache holding only those blocks."""
+    bs_rows = block_tables[rows]
+    used = sorted({int(b) for r, n in zip(bs_rows.tolist(), lens) for b in r[:n] if b >= 0})
+    remap = {b: i for i, b in enumerate(used)}
+    table = np.full(bs_rows.shape, -1, np.int32)
+    for i, (r, n) in enumerate(zip(bs_rows.tolist(), lens)):
+        for j in range(n):
+            table[i, j] = remap[r[j]]
+    return used, table
+
+
+def test_decode_large_padded_sampled():
+    """Batch 256 + 32 padding rows, GQA group 4, lognormal contexts up to 32k,
+    40000-block pool (40 GiB of K/V on the device): checked on sampled rows."""
+    work = W.large_decode()
+    h = work.heads
+    lens = work.context_lens.numpy()
+    rng = np.random.default_rng(5)
+    rows = sorted(set([int(np.argmax(lens)), int(np.argmin(lens[:256])), 256, 287] +
+                      rng.choice(256, 12, replace=False).tolist()))
+    nblk = [int((lens[r] + h.block_size - 1) // h.block_size) for r in rows]
+    used, table = _compact_blocks(work.block_tables.numpy(), rows, nblk)
+    shape = (h.num_blocks, h.block_size, h.num_kv_heads, h.head_dim)
+    gk = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    gv = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    W.fill_normal_(gk, 501)
+    W.fill_normal_(gv, 502)
+    # the oracle's copy of the history: the seeded values, taken before the
+    # CUDA path writes anything
+    idx = torch.tensor(used, dtype=torch.long, device="cuda")
+    kref, vref = bits(gk[idx]).copy(), bits(gv[idx]).copy()
+    bt, ctx = dev(work.block_tables), dev(work.context_lens)
+    gslots = ops.kv_build_decode_slots(bt, ctx, h.block_size)
+    ops.kv_store(dev(work.k), dev(work.v), gk, gv, gslots)
+    out, lse = ops.paged_attn_decode(dev(work.q), gk, gv, bt, ctx, work.max_context_len, h.scale,
+                                     return_lse=True)
+    torch.cuda.synchronize()
+    sub_ctx = lens[rows]
+    slots = oracle.decode_slots(table, sub_ctx, h.block_size)
+    oracle.kv_store(bits(work.k[rows]), bits(work.v[rows]), kref, vref, slots)
+    ref, ref_lse = oracle.decode(bits(work.q[rows]), kref, vref, table, sub_ctx, h.scale)
+    assert_close(out[rows], ref, "large decode (sampled rows)")
+    got = lse[rows].cpu().double().numpy()
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(got), fin)
+    assert np.allclose(got[fin], ref_lse[fin], atol=2e-3, rtol=1e-4)
+    assert out[256:].eq(0).all()
+    del gk, gv
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# prefill
+# ---------------------------------------------------------------------------
+def _prefill_packed(heads, lens, seed, fused=False):
+    work = W.prefill_work(heads, lens, seed=seed)
+    ref, ref_lse = oracle.prefill(bits(work.q), bits(work.k), bits(work.v), work.cu_seqlens_q,
+                                  work.cu_seqlens_k, heads.scale)
+    if fused:
+        qkv = dev(torch.cat([work.q.flatten(1), work.k.flatten(1), work.v.flatten(1)], 1))
+        qw, kw = heads.num_heads * heads.head_dim, heads.num_kv_heads * heads.head_dim
+        n = work.total_q
+        q = qkv[:, :qw].view(n, heads.num_heads, heads.head_dim)
+        k = qkv[:, qw:qw + kw].view(n, heads.num_kv_heads, heads.head_dim)
+        v = qkv[:, qw + kw:].view(n, heads.num_kv_heads, heads.head_dim)
+    else:
+        q, k, v = dev(work.q), dev(work.k), dev(work.v)
+    out, lse = ops.paged_attn_prefill(q, k, v, dev(work.cu_seqlens_q), dev(work.cu_seqlens_k),
+                                      work.max_seqlen_q, work.max_seqlen_k, heads.scale,
+                                      return_lse=True)
+    torch.cuda.synchronize()
+    assert_close(out, ref, "prefill out")
+    got = lse.cpu().double().numpy()
+    assert np.allclose(got, ref_lse, atol=2e-3, rtol=1e-4)
+
+
+PREFILL_SHAPES = [
+    (16, 8, 128, [1, 127, 128, 129, 300, 0, 17]),
+    (16, 8, 128, [512]),
+    (8, 8, 128, [200, 5]),
+    (16, 4, 128, [130, 64]),
+    (8, 2, 64, [250, 1, 129]),
+]
+
+
+@pytest.mark.parametrize("shape", PREFILL_SHAPES, ids=lambda s: f"{s[0]}q{s[1]}kv{s[2]}d")
+def test_prefill_packed_vs_oracle(shape):
+    hq, hkv, d, lens = shape
+    _prefill_packed(W.Heads(hq, hkv, d, 16, 4), lens, seed=600 + hq + d + len(lens))
+
+
+def test_prefill_fused_qkv_views():
+    _prefill_packed(W.Heads(16, 8, 128, 16, 4), [300, 77], seed=650, fused=True)
+
+
+def _prefill_paged(heads, q_lens, prefix, seed, poison=True):
+    work = W.prefill_work(heads, q_lens, prefix, seed=seed)
+    kc, vc = W.history_cache(heads, seed + 1)
+    if poison:
+        _poison_unused(kc, vc, work.block_tables, work.prefix_lens)   # the chunk is written below
+    kref, vref = bits(kc).copy(), bits(vc).copy()
+    slots = oracle.slot_mapping(work.block_tables, work.prefix_lens, work.cu_seqlens_q,
+                                heads.block_size)
+    oracle.kv_store(bits(work.k), bits(work.v), kref, vref, slots)
+    ref, ref_lse = oracle.prefill(bits(work.q), None, None, work.cu_seqlens_q, work.cu_seqlens_k,
+                                  heads.scale, k_cache=kref, v_cache=vref,
+                                  block_tables=work.block_tables)
+    gk, gv = dev(kc), dev(vc)
+    bt = dev(work.block_tables)
+    gs = ops.kv_build_slot_mapping(bt, dev(work.prefix_lens), dev(work.cu_seqlens_q),
+                                   heads.block_size)
+    ops.kv_store(dev(work.k), dev(work.v), gk, gv, gs)
+    out, lse = ops.paged_attn_prefill(dev(work.q), None, None, dev(work.cu_seqlens_q),
+                                      dev(work.cu_seqlens_k), work.max_seqlen_q, work.max_seqlen_k,
+                                      heads.scale, k_cache=gk, v_cache=gv, block_tables=bt,
+                                      return_lse=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(gs.cpu().numpy(), slots)
+    assert_close(out, ref, "paged prefill out")
+    assert np.allclose(lse.cpu().double().numpy(), ref_lse, atol=2e-3, rtol=1e-4)
+
+
+@pytest.mark.parametrize("bs", [16, 64, 256])
+def test_prefill_prefix_cache_aligned(bs):
+    heads = W.Heads(16, 8, 128, bs, 96 * 256 // bs)
+    _prefill_paged(heads, [100, 300, 1, 64], [2 * bs, 0, 3 * bs, bs], seed=700 + bs)
+
+
+@pytest.mark.parametrize("bs", [16, 256])
+def test_prefill_prefix_cache_unaligned(bs):
+    heads = W.Heads(16, 8, 128, bs, 96 * 256 // bs)
+    _prefill_paged(heads, [100, 257, 7], [bs + 5, 3, 2 * bs + bs - 1], seed=750 + bs)
+
+
+def test_prefill_paged_group4_d64():
+    heads = W.Heads(16, 4, 64, 32, 64)
+    _prefill_paged(heads, [90, 200], [40, 0], seed=780)
+
+
+def test_prefill_varlen_full_size_sampled():
+    """8 prompts of U[128, 4096] tokens (about 16k), packed: sampled rows."""
+    work = W.varlen_prefill()
+    h = work.heads
+    out = ops.paged_attn_prefill(dev(work.q), dev(work.k), dev(work.v), dev(work.cu_seqlens_q),
+                                 dev(work.cu_seqlens_k), work.max_seqlen_q, work.max_seqlen_k,
+                                 h.scale)
+    torch.cuda.synchronize()
+    cu = work.cu_seqlens_q.tolist()
+    rng = np.random.default_rng(11)
+    rows = set(rng.choice(work.total_q, 48, replace=False).tolist())
+    for i in range(work.num_seqs):
+        rows |= {cu[i], cu[i + 1] - 1, min(cu[i] + 128, cu[i + 1] - 1)}
+    rows = sorted(rows)
+    ref, _ = oracle.prefill_rows(bits(work.q), bits(work.k), bits(work.v), work.cu_seqlens_q,
+                                 work.cu_seqlens_k, h.scale, rows)
+    assert_close(out[rows], ref, "varlen prefill (sampled rows)")
+
+
+def test_prefill_prefix_full_size_sampled():
+    """16 sequences, cached prefix of U{0..12} blocks of 256 plus a chunk of
+    U[64, 1024] tokens read through block_tables: sampled rows."""
+    work = W.prefix_prefill()
+    h = work.heads
+    kc, vc = W.history_cache(h, 801)
+    kref, vref = bits(kc).copy(), bits(vc).copy()
+    slots = oracle.slot_mapping(work.block_tables, work.prefix_lens, work.cu_seqlens_q,
+                                h.block_size)
+    oracle.kv_store(bits(work.k), bits(work.v), kref, vref, slots)
+    gk, gv = dev(kc), dev(vc)
+    bt = dev(work.block_tables)
+    gs = ops.kv_build_slot_mapping(bt, dev(work.prefix_lens), dev(work.cu_seqlens_q), h.block_size)
+    ops.kv_store(dev(work.k), dev(work.v), gk, gv, gs)
+    out = ops.paged_attn_prefill(dev(work.q), None, None, dev(work.cu_seqlens_q),
+                                 dev(work.cu_seqlens_k), work.max_seqlen_q, work.max_seqlen_k,
+                                 h.scale, k_cache=gk, v_cache=gv, block_tables=bt)
+    torch.cuda.synchronize()
+    assert np.array_equal(gs.cpu().numpy(), slots)
+    rng = np.random.default_rng(12)
+    cu = work.cu_seqlens_q.tolist()
+    rows = set(rng.choice(work.total_q, 40, replace=False).tolist())
+    for i in range(work.num_seqs):
+        rows |= {cu[i], cu[i + 1] - 1}
+    rows = sorted(rows)
+    ref, _ = oracle.prefill_rows(bits(work.q), None, None, work.cu_seqlens_q, work.cu_seqlens_k,
+                                 h.scale, rows, k_cache=kref, v_cache=vref,
+                                 block_tables=work.block_tables)
+    assert_close(out[rows], ref, "prefix prefill (sampled rows)")
+
+
+def test_prefill_unaligned_prefix_full_size_sampled():
+    work = W.prefix_prefill(unaligned=True)
+    h = work.heads
+    kc, vc = W.history_cache(h, 811)
+    kref, vref = bits(kc).copy(), bits(vc).copy()
+    slots = oracle.slot_mapping(work.block_tables, work.prefix_lens, work.cu_seqlens_q,
+                                h.block_size)
+    oracle.kv_store(bits(work.k), bits(work.v), kref, vref, slots)
+    gk, gv = dev(kc), dev(vc)
+    bt = dev(work.block_tables)
+    gs = ops.kv_build_slot_mapping(bt, dev(work.prefix_lens), dev(work.cu_seqlens_q), h.block_size)
+    ops.kv_store(dev(work.k), dev(work.v), gk, gv, gs)
+    assert np.array_equal(gs.cpu().numpy(), slots)
+    assert np.array_equal(bits(gk), kref) and np.array_equal(bits(gv), vref)
+    out = ops.paged_attn_prefill(dev(work.q), None, None, dev(work.cu_seqlens_q),
+                                 dev(work.cu_seqlens_k), work.max_seqlen_q, work.max_seqlen_k,
+                                 h.scale, k_cache=gk, v_cache=gv, block_tables=bt)
+    torch.cuda.synchronize()
+    cu = work.cu_seqlens_q.tolist()
+    rows = sorted({cu[i] for i in range(work.num_seqs)} | {cu[i + 1] - 1 for i in range(work.num_seqs)})
+    ref, _ = oracle.prefill_rows(bits(work.q), None, None, work.cu_seqlens_q, work.cu_seqlens_k,
+                                 h.scale, rows, k_cache=kref, v_cache=vref,
+                                 block_tables=work.block_tables)
+    assert_close(out[rows], ref, "unaligned prefix prefill (sampled rows)")
+
+
+def test_decode_equals_last_prefill_row_on_gpu():
+    """The invariant of the pages (decode step t sees position t) on the CUDA
+    path itself: decode over ctx tokens equals the last row of a causal
+    prefill over the same tokens, within tolerance."""
+    heads = W.Heads(16, 8, 128, 256, 8)
+    n = 700
+    work = W.prefill_work(heads, [n], seed=900)
+    gk, gv = (t.to("cuda") for t in W.empty_cache(heads))
+    bt = dev(work.block_tables)
+    gs = ops.kv_build_slot_mapping(bt, dev(work.prefix_lens), dev(work.cu_seqlens_q), 256)
+    ops.kv_store(dev(work.k), dev(work.v), gk, gv, gs)
+    full = ops.paged_attn_prefill(dev(work.q), dev(work.k), dev(work.v), dev(work.cu_seqlens_q),
+                                  dev(work.cu_seqlens_k), n, n, heads.scale)
+    dec = ops.paged_attn_decode(dev(work.q[n - 1:n]), gk, gv, bt, dev(torch.tensor([n], dtype=torch.int32)),
+                                n, heads.scale)
+    torch.cuda.synchronize()
+    assert_close(dec[0], full[n - 1].float().cpu().double().numpy(), "decode vs last prefill row")
+
+
+def test_validate_mode_reports_bad_table():
+    ops.set_validate(True)
+    try:
+        bt = dev(torch.tensor([[0, -1]], dtype=torch.int32))
+        with pytest.raises(ops.PagedKVError) as e:
+            ops.kv_build_decode_slots(bt, dev(torch.tensor([6], dtype=torch.int32)), 4)
+        assert e.value.code == 5
+    finally:
+        ops.set_validate(False)

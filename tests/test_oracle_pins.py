@@ -446,3 +446,19 @@ def test_tiny_workload_shape():
     assert pre.total_q == 9 and dec.context_lens.tolist() == [7, 4]
     # decode slot of seq 0: position 6 lives in block 9 at offset 2
     assert oracle.decode_slots(dec.block_tables, dec.context_lens, 4)[0] == 38
+
+
+def test_prefill_rows_equal_full_prefill_rows():
+    heads = W.Heads(4, 2, 16, 4, 32)
+    work = W.prefill_work(heads, [5, 0, 11], [3, 0, 6], seed=81)
+    kc, vc = W.history_cache(heads, 82)
+    kcb, vcb = bits(kc).copy(), bits(vc).copy()
+    slots = oracle.slot_mapping(work.block_tables, work.prefix_lens, work.cu_seqlens_q, 4)
+    oracle.kv_store(bits(work.k), bits(work.v), kcb, vcb, slots)
+    kw = dict(k_cache=kcb, v_cache=vcb, block_tables=work.block_tables)
+    full, full_lse = oracle.prefill(bits(work.q), None, None, work.cu_seqlens_q,
+                                    work.cu_seqlens_k, heads.scale, **kw)
+    rows = [15, 0, 7, 4]
+    part, part_lse = oracle.prefill_rows(bits(work.q), None, None, work.cu_seqlens_q,
+                                         work.cu_seqlens_k, heads.scale, rows, **kw)
+    assert np.array_equal(part, full[rows]) and np.array_equal(part_lse, full_lse[rows])

@@ -230,6 +230,8 @@ int paged_attn_decode(const pkv_bf16 *q, int64_t q_row_stride, const pkv_bf16 *k
         bt_stride < max_blocks_per_seq)
         return fail(PKV_ERR_INVALID_ARG, "%s: negative size or bt_stride < max_blocks_per_seq", what);
     if (batch == 0) return ok();
+    if (block_size & (block_size - 1))
+        return fail(PKV_ERR_UNSUPPORTED, "%s: block_size must be a power of two", what);
     const int G = num_heads / num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8)
         return fail(PKV_ERR_UNSUPPORTED, "%s: num_heads / num_kv_heads must be 1, 2, 4 or 8", what);

@@ -364,11 +364,11 @@ PREFILL_SHAPES = [
 @pytest.mark.parametrize("shape", PREFILL_SHAPES, ids=lambda s: f"{s[0]}q{s[1]}kv{s[2]}d")
 def test_prefill_packed_vs_oracle(shape):
     hq, hkv, d, lens = shape
-    _prefill_packed(W.Heads(hq, hkv, d, 16, 4), lens, seed=600 + hq + d + len(lens))
+    _prefill_packed(W.Heads(hq, hkv, d, 16, 256), lens, seed=600 + hq + d + len(lens))
 
 
 def test_prefill_fused_qkv_views():
-    _prefill_packed(W.Heads(16, 8, 128, 16, 4), [300, 77], seed=650, fused=True)
+    _prefill_packed(W.Heads(16, 8, 128, 16, 256), [300, 77], seed=650, fused=True)
 
 
 def _prefill_paged(heads, q_lens, prefix, seed, poison=True):

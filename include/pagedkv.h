@@ -226,6 +226,39 @@ size_t paged_attn_decode_workspace_size(int32_t batch, int32_t num_heads,
                                         int32_t num_kv_heads, int32_t head_dim,
                                         int32_t max_context_len);
 
+/* ------------------------------------------------------------------------
+ * paged_attn_decode_noalloc -- the pages have no counterpart: this entry
+ * point exists for callers of this library that cannot allocate device
+ * memory, such as a plugin inside a host framework that owns every device
+ * allocation and only passes tensors in, or a runtime that forbids
+ * allocations after start-up.  It computes exactly what paged_attn_decode
+ * computes, with the same arguments minus the workspace: the split partials
+ * go to a static device array of PKV_DECODE_STATIC_SCRATCH_BYTES owned by the
+ * library, which every GPU that loads the library keeps resident until the
+ * process exits.  The caller still passes inputs and outputs.  It calls no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *   - A launch whose paged_attn_decode_workspace_size() exceeds
+ *     PKV_DECODE_STATIC_SCRATCH_BYTES is rejected with PKV_ERR_WORKSPACE and
+ *     a message saying so; nothing is launched.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture on the device.
+ *   - Every call shares the one array, which keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls that can overlap on the
+ *     GPU (different streams, or several host threads, without ordering
+ *     between them) race on it and give wrong results; order them.
+ * ---------------------------------------------------------------------- */
+#define PKV_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
+
+int paged_attn_decode_noalloc(const pkv_bf16 *q, int64_t q_row_stride,
+                              const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, int64_t num_blocks,
+                              const int32_t *block_tables, int64_t bt_stride,
+                              int32_t max_blocks_per_seq, const int32_t *context_lens,
+                              int32_t batch, int32_t num_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t block_size, int32_t max_context_len,
+                              float softmax_scale, pkv_bf16 *out, int64_t out_row_stride,
+                              float *lse, pkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

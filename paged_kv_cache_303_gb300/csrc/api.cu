@@ -85,6 +85,14 @@ EncodeTiledFn encode_fn(const char **err) {
 
 namespace pkv {
 
+int report(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
 int num_sms() {
     static int cached[64];
     int dev = 0;

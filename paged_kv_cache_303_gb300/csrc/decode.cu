@@ -35,6 +35,8 @@
 // (K and V, bf16) + q and out; arithmetic intensity about G FLOP/byte.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -593,3 +595,76 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream, const char **err) {
 }
 
 }  // namespace pkv
+
+// ---------------------------------------------------------------------------
+// Decode without any allocation by the caller.
+//
+// Some callers cannot obtain device memory for the split partials: a plugin
+// running inside a host framework that owns every device allocation and only
+// hands over tensors, or a runtime that forbids allocations after start-up.
+// For them the partials live in a fixed array that belongs to this library
+// and stays resident on every GPU that loads it, until the process exits.
+// Nothing in the array has to start at zero: every partial the merge kernel
+// reads is written earlier in the same call.
+// ---------------------------------------------------------------------------
+namespace pkv {
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)PKV_DECODE_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_decode_static_scratch[kStaticScratchBytes];
+
+// Device address of the array, looked up once per device with that device
+// current (in host code the array's name is only a host-side stand-in, never
+// a device address).
+void *static_scratch_address(const char **err) {
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { *err = cudaGetErrorString(e); return nullptr; }
+    if (dev < 0 || dev >= 64) { *err = "device ordinal out of range"; return nullptr; }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_static_scratch);
+        if (e != cudaSuccess) { *err = cudaGetErrorString(e); return nullptr; }
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" int paged_attn_decode_noalloc(const pkv_bf16 *q, int64_t q_row_stride,
+                                         const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                         int64_t num_blocks, const int32_t *block_tables,
+                                         int64_t bt_stride, int32_t max_blocks_per_seq,
+                                         const int32_t *context_lens, int32_t batch,
+                                         int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t block_size, int32_t max_context_len,
+                                         float softmax_scale, pkv_bf16 *out,
+                                         int64_t out_row_stride, float *lse, pkv_stream_t stream) {
+    const size_t need = paged_attn_decode_workspace_size(batch, num_heads, num_kv_heads, head_dim,
+                                                         max_context_len);
+    if (need > pkv::kStaticScratchBytes)
+        return pkv::report(PKV_ERR_WORKSPACE,
+                           "paged_attn_decode_noalloc: this launch needs %zu bytes of split "
+                           "scratch, more than the %zu-byte static array; use paged_attn_decode "
+                           "with a caller workspace, or a smaller batch*num_heads or "
+                           "max_context_len",
+                           need, pkv::kStaticScratchBytes);
+    void *scratch = nullptr;
+    if (need > 0) {
+        const char *err = "";
+        scratch = pkv::static_scratch_address(&err);
+        if (!scratch)
+            return pkv::report(PKV_ERR_CUDA,
+                               "paged_attn_decode_noalloc: cudaGetSymbolAddress failed: %s", err);
+    }
+    return paged_attn_decode(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables, bt_stride,
+                             max_blocks_per_seq, context_lens, batch, num_heads, num_kv_heads,
+                             head_dim, block_size, max_context_len, softmax_scale, out,
+                             out_row_stride, lse, scratch, scratch ? pkv::kStaticScratchBytes : 0,
+                             stream);
+}

@@ -94,4 +94,7 @@ int encode_rows_heads_map(CUtensorMap *map, const void *base, int64_t rows, int3
 
 int num_sms();
 
+// record an error for pkv_last_error() and return `code`
+int report(int code, const char *fmt, ...);
+
 }  // namespace pkv

@@ -52,6 +52,8 @@ SIGNATURES = {
     "paged_attn_decode": ([_P, _I64, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32, _I32, _I32,
                            _I32, _I32, _F32, _P, _I64, _P, _P, _SZ, _P], _INT),
     "paged_attn_decode_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
+    "paged_attn_decode_noalloc": ([_P, _I64, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32, _I32,
+                                   _I32, _I32, _I32, _F32, _P, _I64, _P, _P], _INT),
 }
 
 _lib = None

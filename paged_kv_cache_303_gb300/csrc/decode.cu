@@ -5,31 +5,31 @@
 //
 // Work unit: one CTA per (kv head, chunk of keys, sequence).  The CTA holds
 // the GQA group's G query vectors (all query heads that share the kv head,
-// §3) in registers, so every K/V byte it reads serves G heads.
+// §3) in shared memory, so every K/V byte it reads serves G heads.
 //
 // Data path:
-//   * K and V of 64 tokens at a time ("tile") are staged into shared memory
+//   * K and V of 32 tokens at a time ("tile") are staged into shared memory
 //     by 3-D TMA over the cache viewed as [num_slots, num_kv_heads, head_dim]
-//     (box: 64 head_dim elements x 1 head x min(block_size, 64) slots).  A
-//     tile of a block_size >= 64 cache is one box per 64-element half of the
-//     head_dim; smaller blocks take one box per block segment.  With
+//     (box: 64 head_dim elements x 1 head x min(block_size, 32) slots).  With
 //     block_size >= 8 the boxes use the 128-byte swizzle so that the
-//     row-per-thread reads below are bank-conflict free.
-//   * A 3-stage mbarrier pipeline keeps two tiles in flight while one is
-//     consumed; thread 0 refills a stage as soon as the whole CTA has left it.
-//   * Scores: each token is owned by TPT consecutive threads that each dot a
-//     slice of head_dim with the G queries (packed fp32x2 FMAs) and combine
-//     by shuffles.  Scores carry scale*log2(e) so the softmax uses exp2.
-//   * Softmax: the CTA-wide tile maximum updates the running maximum m; the
-//     running sum l and output accumulators are rescaled by 2^(m_old-m_new)
-//     (§5.2's exact rescaling).  Probabilities go to shared memory.
-//   * P.V: each thread owns 8 head_dim elements of a group of tokens; tokens
-//     whose probabilities are all zero (masked tail, invalid block) are
-//     skipped, so garbage in unwritten cache slots never reaches the sum.
-//   * Epilogue: a single-chunk launch writes bf16 out and lse directly;
-//     otherwise each CTA writes (m, l, unnormalised o) in fp32 to the
-//     workspace and decode_combine_kernel merges the chunks of each
-//     (sequence, head).
+//     row-per-lane reads below are bank-conflict free.
+//   * One producer warp keeps a ring of stages full (an mbarrier pair per
+//     stage); the consumer warps each take whole tiles in turn, with no
+//     CTA-wide barrier inside the loop.
+//   * Scores: lane = token; the lane dots its key row with the G queries
+//     (packed fp32x2 FMAs).  Scores carry scale*log2(e) so the softmax uses
+//     exp2.
+//   * Softmax: per warp and head, the tile maximum (shuffles) updates the
+//     warp's running maximum m; its running sum l and output accumulators are
+//     rescaled by 2^(m_old-m_new) (§5.2's exact rescaling).
+//   * P.V: lane = head_dim/32 elements of every value row; in a tile that is
+//     not complete (sequence tail, missing block) tokens whose probabilities
+//     are all zero are skipped, so garbage in unwritten cache slots never
+//     reaches the sum.
+//   * The consumer warps' (m, l, o) are merged once per chunk; a
+//     single-chunk launch writes bf16 out and lse directly, otherwise each CTA
+//     writes (m, l, unnormalised o) in fp32 to the workspace and
+//     decode_combine_kernel merges the chunks of each (sequence, head).
 //
 // Bound: HBM.  Algorithmic bytes per launch = sum_b ctx_b * Hkv * d * 2 * 2
 // (K and V, bf16) + q and out; arithmetic intensity about G FLOP/byte.
@@ -61,10 +61,20 @@ cudaError_t decode_status(cudaStream_t stream, uint32_t *host, bool clear) {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kTile = 64;      // tokens per pipeline stage
-constexpr int kStages = 3;
+// Tunables (compile-time): consumer warps per CTA, ring depth, CTAs per SM.
+#ifndef PKV_DEC_CONSUMERS
+#define PKV_DEC_CONSUMERS 4
+#endif
+#ifndef PKV_DEC_STAGES
+#define PKV_DEC_STAGES 6
+#endif
+#ifndef PKV_DEC_MIN_CTAS
+#define PKV_DEC_MIN_CTAS 2
+#endif
+constexpr int kConsumers = PKV_DEC_CONSUMERS;    // consumer warps per CTA
+constexpr int kThreads = (kConsumers + 1) * 32;  // + one TMA producer warp
+constexpr int kTile = 32;                        // tokens per pipeline stage (one per lane)
+constexpr int kStages = PKV_DEC_STAGES;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -86,12 +96,19 @@ struct DecodeParams {
     float *part_ml;            // [B, Hq, S, 2]  fp32 (split mode)
 };
 
-template <int HD>
+template <int HD, int G>
 struct Layout {
     static constexpr int kHalves = HD / 64;                      // 128-byte rows per head_dim
     static constexpr int kTileBytes = kHalves * kTile * 128;     // one of K or V
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kPipeBytes = kStages * kStageBytes;
+    static constexpr int kOffBar = kPipeBytes;                   // full[S], empty[S], masks, abort
+    static constexpr int kOffQ = kOffBar + 256;                  // q, fp32 [G][HD]
+    static constexpr int kOffP = kOffQ + G * HD * 4;             // probabilities [warp][G][kTile]
+    static constexpr int kBytes = kOffP + kConsumers * G * kTile * 4;
+    // end-of-chunk merge buffers reuse the pipeline
+    static_assert(kConsumers * G * (HD + 2) * 4 <= kPipeBytes, "merge buffer must fit");
+    static_assert(kStages * 20 + 4 <= 256, "barrier area");
 };
 
 template <bool SW>
@@ -99,29 +116,49 @@ __device__ __forceinline__ uint32_t chunk_off(int row, int chunk) {
     return row * 128 + ((SW ? (chunk ^ (row & 7)) : chunk) << 4);
 }
 
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+}
+
+// Wait that gives up when another warp has aborted, or after the time bound
+// (then it raises the abort flag itself).
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            *abort_flag = 1;
+            atomicOr(&g_decode_status, PKV_STATUS_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Roles: warps 0..kConsumers-1 consume tiles (tile i -> warp i % kConsumers,
+// stage i % kStages); warp kConsumers is the TMA producer.  A consumer warp
+// owns a whole tile: lane = token for the scores, lane = HD/32 head_dim
+// elements for P.V, and keeps its own (m, l, o) for the G heads; the warps'
+// states are merged once at the end of the chunk.
 template <int HD, int G, bool SW>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, PKV_DEC_MIN_CTAS)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
-    using L = Layout<HD>;
-    constexpr int TPT = (G <= 2) ? 4 : 8;           // threads per token in the score phase
-    constexpr int E = HD / TPT;                     // head_dim elements per score thread
-    constexpr int EC = E / 8;                       // 16-byte chunks per score thread
-    constexpr int TOK_PASS = kThreads / TPT;        // tokens per score pass
-    constexpr int PASSES = kTile / TOK_PASS;
-    constexpr int CPR = HD / 8;                     // 16-byte chunks per row (P.V phase)
-    constexpr int GROUPS = kThreads / CPR;          // token groups in the P.V phase
-    constexpr int TPG = kTile / GROUPS;             // tokens per group per tile
-    static_assert(PASSES >= 1 && TPG >= 1 && EC >= 1, "shape");
+    using L = Layout<HD, G>;
+    constexpr int DPL = HD / 32;                    // head_dim elements per lane in P.V
+    constexpr int CPR = HD / 8;                     // 16-byte chunks per K row
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *pipe = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kPipeBytes);
-    float *probs = reinterpret_cast<float *>(smem + L::kPipeBytes + 64);      // [G][kTile]
-    float *red = probs + G * kTile;                                           // [kWarps][G]
-    float *lred = red + kWarps * G;                                           // [kWarps][G]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
+    uint64_t *empty = full + kStages;
+    uint32_t *seg_valid = reinterpret_cast<uint32_t *>(empty + kStages);   // [kStages]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(seg_valid + kStages);
+    float *qs = reinterpret_cast<float *>(smem + L::kOffQ);
+    float *ps = reinterpret_cast<float *>(smem + L::kOffP);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -130,8 +167,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     const int split = blockIdx.y;
     const int b = blockIdx.z;
     const int hq0 = kvh * G;
-    const int S = p.max_splits;
-    const bool direct = (S == 1);
+    const bool direct = (p.max_splits == 1);
 
     int ctx = p.ctx[b];
     if (ctx < 0 || ctx > p.max_context_len) {
@@ -155,41 +191,37 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     const int32_t *bt_row = p.bt + (int64_t)b * p.bt_stride;
     const int bs = p.block_size;
     const int TB = bs < kTile ? bs : kTile;          // slots per TMA box
+
+    // TMA producer (one lane of the last warp): stage tile i into stage i % kStages
     const uint32_t box_bytes = (uint32_t)TB * 128u;
-
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
-        fence_barrier_init();
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&vmap);
-    }
-    __syncthreads();
-
-    const uint64_t policy = policy_evict_first();
-    // thread 0: stage tile `i` into its stage
-    auto issue = [&](int i) {
+    auto issue = [&](int i, uint64_t policy) {
         const int stage = i % kStages;
         const int p0 = tok_begin + i * kTile;
         const int nv = min(kTile, tok_end - p0);
         const int nseg = (nv + TB - 1) / TB;
         int ok = 0;
+        uint32_t mask = 0;               // bit sg: segment sg was loaded
         for (int sg = 0; sg < nseg; ++sg) {
             const int pos = p0 + sg * TB;
             const int lb = pos / bs;
             const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
-            if (blk >= 0 && blk < p.num_blocks) ++ok;
+            if (blk >= 0 && blk < p.num_blocks) {
+                ++ok;
+                mask |= 1u << sg;
+            }
         }
+        // published to the consumers by the release of the arrive below
+        seg_valid[stage] = mask;
         mbar_arrive_expect_tx(&full[stage], (uint32_t)ok * L::kHalves * 2u * box_bytes);
         unsigned char *kdst = pipe + stage * L::kStageBytes;
         unsigned char *vdst = kdst + L::kTileBytes;
         for (int sg = 0; sg < nseg; ++sg) {
-            const int pos = p0 + sg * TB;
-            const int lb = pos / bs;
-            const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
-            if (blk < 0 || blk >= p.num_blocks) {
+            if (!((mask >> sg) & 1u)) {
                 atomicOr(&g_decode_status, PKV_STATUS_BAD_BLOCK);
                 continue;
             }
+            const int pos = p0 + sg * TB;
+            const int blk = bt_row[pos / bs];
             const int z = (int)((int64_t)blk * bs + pos % bs);
 #pragma unroll
             for (int hf = 0; hf < L::kHalves; ++hf) {
@@ -199,228 +231,237 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             }
         }
     };
-    if (tid == 0) {
-        for (int i = 0; i < kStages && i < ntiles; ++i) issue(i);
-    }
+    const int prologue = ntiles < kStages ? ntiles : kStages;
 
-    // ---- this thread's query slice, pre-scaled by scale*log2(e) ----
-    const int qd = tid % TPT;                       // slice of head_dim in the score phase
-    const int e0 = qd * E;
-    float2 q2[G][E / 2];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const uint16_t *qrow = p.q + (int64_t)b * p.q_rs + (int64_t)(hq0 + h) * HD + e0;
-#pragma unroll
-        for (int c = 0; c < EC; ++c) {
-            const uint4 w = *reinterpret_cast<const uint4 *>(qrow + c * 8);
+    if (warp == kConsumers) {
+        // the producer starts the first kStages tiles before anything else,
+        // so that their latency overlaps the query load below
+        if (lane == 0) {
+            for (int s = 0; s < kStages; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], 1);
+            }
+            *abort_flag = 0;
+            fence_barrier_init();
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
+            const uint64_t policy = policy_evict_first();
+            for (int i = 0; i < prologue; ++i) issue(i, policy);
+        }
+    } else {
+        // the G query vectors of this kv head, scaled by scale*log2(e), as fp32
+        for (int i = tid; i < G * HD / 8; i += kConsumers * 32) {
+            const int h = i / (HD / 8), c = i % (HD / 8);
+            const uint4 w = *reinterpret_cast<const uint4 *>(p.q + (int64_t)b * p.q_rs +
+                                                             (int64_t)(hq0 + h) * HD + c * 8);
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            float *dst = qs + h * HD + c * 8;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                q2[h][c * 4 + k] = make_float2(bf16lo_to_f32(ws[k]) * p.scale_log2,
-                                               bf16hi_to_f32(ws[k]) * p.scale_log2);
+            for (int k = 0; k < 4; ++k) {
+                dst[2 * k] = bf16lo_to_f32(ws[k]) * p.scale_log2;
+                dst[2 * k + 1] = bf16hi_to_f32(ws[k]) * p.scale_log2;
+            }
         }
     }
+    __syncthreads();
 
-    // P.V role of this thread
-    const int pv_chunk = tid % CPR;                 // 8-element chunk of head_dim
-    const int pv_group = tid / CPR;                 // token group
-    const int pv_half = pv_chunk / 8;
-    const int pv_c = pv_chunk % 8;
+    if (warp == kConsumers) {
+        if (lane == 0) {
+            const uint64_t policy = policy_evict_first();
+            int issued = prologue;
+            for (int i = prologue; i < ntiles; ++i) {
+                const int stage = i % kStages;
+                if (!wait_or_abort(&empty[stage], (uint32_t)((i / kStages) - 1) & 1u, abort_flag))
+                    break;
+                issue(i, policy);
+                ++issued;
+            }
+            // no copy may still be landing when the CTA exits
+            for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+                (void)mbar_wait(&full[j % kStages], (uint32_t)(j / kStages) & 1u);
+        }
+        return;
+    }
 
+    // ----------------------------------------------------------------------
+    // consumer warps
+    // ----------------------------------------------------------------------
     float m_run[G], l_part[G];
-    float2 o2[G][4];
+    float2 o2[G][DPL / 2];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         m_run[h] = -INFINITY;
         l_part[h] = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) o2[h][k] = make_float2(0.f, 0.f);
+        for (int k = 0; k < DPL / 2; ++k) o2[h][k] = make_float2(0.f, 0.f);
     }
+    float *pw = ps + warp * G * kTile;             // this warp's probabilities [G][kTile]
+    // this lane's slice of a value row: head_dim elements [lane*DPL, lane*DPL+DPL)
+    const int v_half = (lane * DPL) / 64;
+    const int v_chunk = ((lane * DPL) % 64) / 8;
+    const int v_byte = ((lane * DPL) % 8) * 2;
+    const uint32_t all_segs = kTile / TB >= 32 ? 0xffffffffu : ((1u << (kTile / TB)) - 1u);
 
-    bool aborted = false;
-    for (int i = 0; i < ntiles; ++i) {
+    for (int i = warp; i < ntiles; i += kConsumers) {
         const int stage = i % kStages;
-        const uint32_t parity = (uint32_t)(i / kStages) & 1u;
-        const bool ok = mbar_wait(&full[stage], parity);
+        if (!wait_or_abort(&full[stage], (uint32_t)(i / kStages) & 1u, abort_flag)) break;
         const unsigned char *ktile = pipe + stage * L::kStageBytes;
         const unsigned char *vtile = ktile + L::kTileBytes;
         const int p0 = tok_begin + i * kTile;
 
-        // ---- scores for this thread's token(s) ----
-        float s_tok[PASSES][G];
-        float tmax[G];
+        // ---- scores: lane = token ----
+        float2 acc[G][2];
 #pragma unroll
-        for (int h = 0; h < G; ++h) tmax[h] = -INFINITY;
-#pragma unroll
-        for (int ps = 0; ps < PASSES; ++ps) {
-            const int r = ps * TOK_PASS + tid / TPT;
-            float2 acc[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int c = 0; c < EC; ++c) {
-                const int gchunk = (e0 / 8) + c;                 // chunk index within the row
-                const int hf = gchunk / 8;
-                const uint4 w = *reinterpret_cast<const uint4 *>(
-                    ktile + hf * kTile * 128 + chunk_off<SW>(r, gchunk % 8));
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 kf = make_float2(bf16lo_to_f32(ws[k]), bf16hi_to_f32(ws[k]));
-#pragma unroll
-                    for (int h = 0; h < G; ++h) acc[h] = ffma2(q2[h][c * 4 + k], kf, acc[h]);
-                }
-            }
-            const int pos = p0 + r;
-            bool valid = pos < tok_end;
-            if (valid) {
-                const int lb = pos / bs;
-                const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
-                valid = blk >= 0 && blk < p.num_blocks;
-            }
+        for (int h = 0; h < G; ++h) acc[h][0] = acc[h][1] = make_float2(0.f, 0.f);
+#pragma unroll 4
+        for (int c = 0; c < CPR; ++c) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(ktile + (c / 8) * kTile * 128 +
+                                                             chunk_off<SW>(lane, c % 8));
+            const float2 k0 = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
+            const float2 k1 = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
+            const float2 k2 = make_float2(bf16lo_to_f32(w.z), bf16hi_to_f32(w.z));
+            const float2 k3 = make_float2(bf16lo_to_f32(w.w), bf16hi_to_f32(w.w));
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                float s = acc[h].x + acc[h].y;
-#pragma unroll
-                for (int off = 1; off < TPT; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                s = valid ? s : -INFINITY;
-                s_tok[ps][h] = s;
-                tmax[h] = fmaxf(tmax[h], s);
+                const float4 qa = *reinterpret_cast<const float4 *>(qs + h * HD + c * 8);
+                const float4 qb = *reinterpret_cast<const float4 *>(qs + h * HD + c * 8 + 4);
+                acc[h][0] = ffma2(make_float2(qa.x, qa.y), k0, acc[h][0]);
+                acc[h][1] = ffma2(make_float2(qa.z, qa.w), k1, acc[h][1]);
+                acc[h][0] = ffma2(make_float2(qb.x, qb.y), k2, acc[h][0]);
+                acc[h][1] = ffma2(make_float2(qb.z, qb.w), k3, acc[h][1]);
             }
         }
-        // CTA-wide tile maximum
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float v = tmax[h];
-#pragma unroll
-            for (int off = TPT; off < 32; off <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-            if (lane == 0) red[warp * G + h] = v;
-        }
-        if (__syncthreads_or(!ok)) { aborted = true; break; }
-        // every thread has left tile i-1: refill its stage
-        if (tid == 0 && i >= 1 && i - 1 + kStages < ntiles) issue(i - 1 + kStages);
+        const uint32_t mask = seg_valid[stage];
+        const bool valid = (p0 + lane < tok_end) && ((mask >> (lane / TB)) & 1u);
+        // complete tile: every token present and loaded (warp-uniform)
+        const bool full_tile = (p0 + kTile <= tok_end) && mask == all_segs;
 
-        float alpha[G], m_use[G];
+        // ---- online softmax over the warp's tile ----
+        float alpha[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float v = red[h];
+            const float s = valid ? (acc[h][0].x + acc[h][0].y) + (acc[h][1].x + acc[h][1].y)
+                                  : -INFINITY;
+            float mt = s;
 #pragma unroll
-            for (int w = 1; w < kWarps; ++w) v = fmaxf(v, red[w * G + h]);
-            const float m_new = fmaxf(m_run[h], v);
-            m_use[h] = (m_new == -INFINITY) ? 0.f : m_new;
-            alpha[h] = fast_exp2(m_run[h] - m_use[h]);     // 0 when m_run is -inf
+            for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+            const float m_new = fmaxf(m_run[h], mt);
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            alpha[h] = fast_exp2(m_run[h] - m_use);        // 0 while m_run is -inf
             m_run[h] = m_new;
-            l_part[h] *= alpha[h];
+            const float pr = fast_exp2(s - m_use);
+            l_part[h] = l_part[h] * alpha[h] + pr;
+            pw[h * kTile + lane] = pr;
         }
-        if (qd == 0) {
+        __syncwarp();
+
+        // ---- P.V: lane = DPL head_dim elements ----
 #pragma unroll
-            for (int ps = 0; ps < PASSES; ++ps) {
-                const int r = ps * TOK_PASS + tid / TPT;
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int k = 0; k < DPL / 2; ++k) o2[h][k] = fmul2(o2[h][k], make_float2(alpha[h], alpha[h]));
+        const unsigned char *vrow0 = vtile + v_half * kTile * 128 + v_byte;
+        auto pv_token = [&](int t, const float (&pr)[G]) {
+            const unsigned char *src = vrow0 + chunk_off<SW>(t, v_chunk);
+            if constexpr (DPL == 4) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(src);
+                const float2 v0 = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
+                const float2 v1 = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    const float pr = fast_exp2(s_tok[ps][h] - m_use[h]);
-                    probs[h * kTile + r] = pr;
-                    l_part[h] += pr;
+                    const float2 pp = make_float2(pr[h], pr[h]);
+                    o2[h][0] = ffma2(pp, v0, o2[h][0]);
+                    o2[h][1] = ffma2(pp, v1, o2[h][1]);
+                }
+            } else {
+                const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
+                const float2 v0 = make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w));
+#pragma unroll
+                for (int h = 0; h < G; ++h) o2[h][0] = ffma2(make_float2(pr[h], pr[h]), v0, o2[h][0]);
+            }
+        };
+        if (full_tile) {
+#pragma unroll 2
+            for (int t4 = 0; t4 < kTile; t4 += 4) {
+                float4 pq[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) pq[h] = *reinterpret_cast<const float4 *>(pw + h * kTile + t4);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float pr[G];
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+                        pr[h] = u == 0 ? pq[h].x : u == 1 ? pq[h].y : u == 2 ? pq[h].z : pq[h].w;
+                    pv_token(t4 + u, pr);
                 }
             }
-        }
-        __syncthreads();
-
-        // ---- P.V ----
+        } else {
+            // sequence tail or missing segment: skip tokens whose
+            // probabilities are all zero, so rows that were not loaded (or
+            // hold unwritten cache slots) never reach the sum
+            for (int t = 0; t < kTile; ++t) {
+                float pr[G];
+                bool any = false;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float2 a2 = make_float2(alpha[h], alpha[h]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) o2[h][k] = make_float2(o2[h][k].x * a2.x, o2[h][k].y * a2.y);
-        }
-        const unsigned char *vbase = vtile + pv_half * kTile * 128;
-#pragma unroll
-        for (int t = 0; t < TPG; ++t) {
-            const int r = pv_group * TPG + t;
-            float pr[G];
-            bool any = false;
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                pr[h] = probs[h * kTile + r];
-                any |= pr[h] != 0.f;
-            }
-            if (!any) continue;
-            const uint4 w = *reinterpret_cast<const uint4 *>(vbase + chunk_off<SW>(r, pv_c));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 vf = make_float2(bf16lo_to_f32(ws[k]), bf16hi_to_f32(ws[k]));
-#pragma unroll
-                for (int h = 0; h < G; ++h) o2[h][k] = ffma2(make_float2(pr[h], pr[h]), vf, o2[h][k]);
+                for (int h = 0; h < G; ++h) {
+                    pr[h] = pw[h * kTile + t];
+                    any |= pr[h] != 0.f;
+                }
+                if (any) pv_token(t, pr);        // warp-uniform
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
     }
 
-    if (aborted) {
-        if (tid == 0) {
-            atomicOr(&g_decode_status, PKV_STATUS_TIMEOUT);
-            // let copies already in flight land before the CTA's shared memory is released
-            for (int i = 0; i < ntiles && i < kStages; ++i) {
-                (void)mbar_wait(&full[i % kStages], 0);
-            }
-        }
-        return;
-    }
-
-    // ---- reduce accumulators over token groups ----
-    __syncthreads();                                 // all P.V reads of the pipeline are done
-    float *ored = reinterpret_cast<float *>(pipe);   // [kWarps][G][HD], reuses the pipeline
+    // ---- merge the consumer warps' states ----
+    consumer_sync();                                   // every warp is done with the pipeline
+    const bool aborted = *abort_flag != 0;
+    float *mo = reinterpret_cast<float *>(pipe);       // [warp][G][HD]
+    float *mml = mo + kConsumers * G * HD;             // [warp][G][2]
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float2 v = o2[h][k];
-#pragma unroll
-            for (int off = CPR; off < 32; off <<= 1) {
-                v.x += __shfl_xor_sync(0xffffffffu, v.x, off);
-                v.y += __shfl_xor_sync(0xffffffffu, v.y, off);
-            }
-            o2[h][k] = v;
-        }
         float l = l_part[h];
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-        if (lane == 0) lred[warp * G + h] = l;
-    }
-    if (lane < CPR) {
+        for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        if (lane == 0) {
+            mml[(warp * G + h) * 2] = m_run[h];
+            mml[(warp * G + h) * 2 + 1] = l;
+        }
+        float *dst = mo + (warp * G + h) * HD + lane * DPL;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float *dst = ored + (warp * G + h) * HD + pv_chunk * 8;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                dst[2 * k] = o2[h][k].x;
-                dst[2 * k + 1] = o2[h][k].y;
-            }
+        for (int k = 0; k < DPL / 2; ++k) {
+            dst[2 * k] = o2[h][k].x;
+            dst[2 * k + 1] = o2[h][k].y;
         }
     }
-    __syncthreads();
-    for (int idx = tid; idx < G * HD; idx += kThreads) {
+    consumer_sync();
+    if (aborted) return;
+    for (int idx = tid; idx < G * HD; idx += kConsumers * 32) {
         const int h = idx / HD, e = idx % HD;
+        float m = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) m = fmaxf(m, mml[(w * G + h) * 2]);
+        const float mu = (m == -INFINITY) ? 0.f : m;
         float o = 0.f, l = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            o += ored[(w * G + h) * HD + e];
-            l += lred[w * G + h];
+        for (int w = 0; w < kConsumers; ++w) {
+            const float f = fast_exp2(mml[(w * G + h) * 2] - mu);
+            l += f * mml[(w * G + h) * 2 + 1];
+            o += f * mo[(w * G + h) * HD + e];
         }
         const int hq = hq0 + h;
         if (direct) {
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const float r = o * inv;
             p.out[(int64_t)b * p.out_rs + (int64_t)hq * HD + e] =
-                (uint16_t)(pack_bf16x2(r, 0.f) & 0xffffu);
+                (uint16_t)(pack_bf16x2(o * inv, 0.f) & 0xffffu);
             if (p.lse && e == 0)
-                p.lse[(int64_t)b * p.num_heads + hq] =
-                    l > 0.f ? (m_run[h] + log2f(l)) * kLn2 : -INFINITY;
+                p.lse[(int64_t)b * p.num_heads + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         } else {
-            const int64_t part = ((int64_t)b * p.num_heads + hq) * S + split;
+            const int64_t part = ((int64_t)b * p.num_heads + hq) * p.max_splits + split;
             p.part_o[part * HD + e] = o;
             if (e == 0) {
-                p.part_ml[part * 2] = m_run[h];
+                p.part_ml[part * 2] = m;
                 p.part_ml[part * 2 + 1] = l;
             }
         }
@@ -465,18 +506,11 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
         p.lse[(int64_t)b * p.num_heads + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
-template <int HD>
-constexpr size_t split_smem_bytes(int G) {
-    return 1024 /*alignment slack*/ + Layout<HD>::kPipeBytes + 64 +
-           sizeof(float) * (G * kTile + 2 * kWarps * G);
-}
-
 template <int HD, int G, bool SW>
 int launch_split(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &p, int batch,
                  int num_kv_heads, cudaStream_t stream, const char **err) {
     auto kern = decode_split_kernel<HD, G, SW>;
-    const size_t smem = split_smem_bytes<HD>(G);
-    static_assert(Layout<HD>::kPipeBytes >= kWarps * 8 * HD * 4, "reduction buffer must fit");
+    const size_t smem = 1024 /*alignment slack*/ + Layout<HD, G>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
     dim3 grid(num_kv_heads, p.max_splits, batch);
@@ -503,13 +537,13 @@ int dispatch_group(int G, const CUtensorMap &km, const CUtensorMap &vm, const De
 void decode_plan(int32_t batch, int32_t num_kv_heads, int32_t head_dim, int32_t max_context_len,
                  int32_t *chunk, int32_t *max_splits) {
     (void)head_dim;
-    const int64_t tiles = (int64_t)batch * num_kv_heads * ((max_context_len + kTile - 1) / kTile);
-    // aim for about four waves of two CTAs per SM, assuming contexts average
-    // about half of the maximum
+    // about four waves of two CTAs per SM, assuming contexts average half of
+    // the maximum; chunks of 256 .. 4096 keys
+    const int64_t keys = (int64_t)batch * num_kv_heads * max_context_len / 2;
     const int64_t target = (int64_t)num_sms() * 2 * 4;
-    int64_t per = (tiles / 2 + target - 1) / (target > 0 ? target : 1);
-    if (per < 4) per = 4;
-    if (per > 64) per = 64;
+    int64_t per = (keys + target * kTile - 1) / (target * kTile);
+    if (per < 8) per = 8;
+    if (per > 128) per = 128;
     if (const char *env = getenv("PKV_DECODE_CHUNK_TILES")) {
         const int v = atoi(env);
         if (v >= 1 && v <= 4096) per = v;

@@ -13,9 +13,10 @@
 //     (box: 64 head_dim elements x 1 head x min(block_size, 32) slots).  With
 //     block_size >= 8 the boxes use the 128-byte swizzle so that the
 //     row-per-lane reads below are bank-conflict free.
-//   * One producer warp keeps a ring of stages full (an mbarrier pair per
-//     stage); the consumer warps each take whole tiles in turn, with no
-//     CTA-wide barrier inside the loop.
+//   * One producer warp keeps a 4-stage ring full (an mbarrier pair per
+//     stage); three consumer warps each take whole tiles in turn, with no
+//     CTA-wide barrier inside the loop.  Three CTAs share an SM, so that one
+//     CTA's start-up and merge overlap the others' streaming.
 //   * Scores: lane = token; the lane dots its key row with the G queries
 //     (packed fp32x2 FMAs).  Scores carry scale*log2(e) so the softmax uses
 //     exp2.
@@ -63,13 +64,13 @@ namespace {
 
 // Tunables (compile-time): consumer warps per CTA, ring depth, CTAs per SM.
 #ifndef PKV_DEC_CONSUMERS
-#define PKV_DEC_CONSUMERS 4
+#define PKV_DEC_CONSUMERS 3
 #endif
 #ifndef PKV_DEC_STAGES
-#define PKV_DEC_STAGES 6
+#define PKV_DEC_STAGES 4
 #endif
 #ifndef PKV_DEC_MIN_CTAS
-#define PKV_DEC_MIN_CTAS 2
+#define PKV_DEC_MIN_CTAS 3
 #endif
 constexpr int kConsumers = PKV_DEC_CONSUMERS;    // consumer warps per CTA
 constexpr int kThreads = (kConsumers + 1) * 32;  // + one TMA producer warp
@@ -537,10 +538,10 @@ int dispatch_group(int G, const CUtensorMap &km, const CUtensorMap &vm, const De
 void decode_plan(int32_t batch, int32_t num_kv_heads, int32_t head_dim, int32_t max_context_len,
                  int32_t *chunk, int32_t *max_splits) {
     (void)head_dim;
-    // about four waves of two CTAs per SM, assuming contexts average half of
+    // about three waves of resident CTAs, assuming contexts average half of
     // the maximum; chunks of 256 .. 4096 keys
     const int64_t keys = (int64_t)batch * num_kv_heads * max_context_len / 2;
-    const int64_t target = (int64_t)num_sms() * 2 * 4;
+    const int64_t target = (int64_t)num_sms() * PKV_DEC_MIN_CTAS * 3;
     int64_t per = (keys + target * kTile - 1) / (target * kTile);
     if (per < 8) per = 8;
     if (per > 128) per = 128;

@@ -15,11 +15,17 @@
 //   warp 8     TMA producer: Q once, then K and V tiles of 64 keys through a
 //              3-stage ring (packed k/v: one box per half of head_dim; paged
 //              cache: one box per block segment, addressed via block_tables)
-//   warp 9     MMA issuer: S = Q K^T (M=128, N=64, K=head_dim) into TMEM, and
-//              O += P V (M=128, N=head_dim, K=64) with O resident in TMEM
+//   warp 9     MMA issuer: iteration j issues S_j = Q K_j^T (M=128, N=64,
+//              K=head_dim) for both heads, then O += P_{j-1} V_{j-1}
+//              (M=128, N=head_dim, K=64), so the next scores are computed
+//              while the softmax warps work on the current ones
 //
-// Tensor memory (fp32 accumulators, lane = query row):
-//   S_A cols [0,64), S_B [64,128), O_A [128,128+d), O_B [128+d,128+2d)
+// Tensor memory (fp32 accumulators, lane = query row), 512 columns:
+//   S[head][buffer] at 64*(2*head+buffer), two buffers per head;
+//   O_A at 256, O_B at 256+d.
+// P is double-buffered per head in shared memory too: the softmax of tile j
+// writes buffer j%2, which the P V of tile j-2 has released.  Barrier
+// arrivals from the softmax warpgroups are one per warp.
 //
 // Shared-memory operands use the 128-byte swizzle written by TMA: Q, K and P
 // are K-major, V is read as an MN-major B operand (keys are K, head_dim N).
@@ -27,10 +33,10 @@
 // Softmax: per row, scores are scaled by scale*log2(e) and exponentiated
 // with exp2.  The running maximum is only moved when a tile's maximum
 // exceeds it by more than 8 (a factor 256): then l and the O accumulator
-// in TMEM are rescaled by 2^(m_old - m_new) (§5.2's identity).  Otherwise
-// the stale maximum is kept; every p is then <= 2^8, and the final O / l
-// uses the same maximum for numerator and denominator, so the result is the
-// same softmax.
+// in TMEM are rescaled by 2^(m_old - m_new) (§5.2's identity), after the
+// earlier P V products have landed.  Otherwise the stale maximum is kept;
+// every p is then <= 2^8, and the final O / l uses the same maximum for
+// numerator and denominator, so the result is the same softmax.
 //
 // Causality: query row t of a sequence with Lq queries and Lk keys sees keys
 // j <= Lk - Lq + t.  KV tiles past the last row's bound are never loaded;
@@ -67,8 +73,8 @@ cudaError_t prefill_status(cudaStream_t stream, uint32_t *host, bool clear) {
 namespace {
 
 constexpr int kBM = 128;          // query rows per tile
-constexpr int kBN = 64;           // keys per KV tile
-constexpr int kStages = 3;
+constexpr int kBN = 128;          // keys per KV tile
+constexpr int kSlots = 4;         // ring of K / V tiles (K_j, V_j, K_j+1, ...)
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -173,6 +179,38 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         : "memory");
 }
 
+// 128 consecutive TMEM columns of this warp's 32 lanes -> 128 registers (waits)
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%129];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+        : "r"(taddr), "r"(taddr + 64u)
+        : "memory");
+}
+
+// 32 registers -> 32 consecutive TMEM columns of this warp's lanes (no wait)
+__device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// D (TMEM) += A (TMEM, K-major) * B (shared memory descriptor)
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -268,16 +306,14 @@ template <int HD>
 struct PLayout {
     static constexpr int H = HD / 64;                       // 128-byte halves of a row
     static constexpr int kQTile = H * kBM * 128;            // one query head's tile
-    static constexpr int kKTile = H * kBN * 128;            // K or V tile
-    static constexpr int kStage = 2 * kKTile;
-    static constexpr int kPTile = kBM * 128;                // 128 rows x 64 keys bf16
-    static constexpr int kOffKV = 2 * kQTile;
-    static constexpr int kOffP = kOffKV + kStages * kStage;
-    static constexpr int kOffBar = kOffP + 2 * kPTile;
+    static constexpr int kKVTile = H * kBN * 128;           // one K or V tile (a ring slot)
+    static constexpr int kOffRing = 2 * kQTile;
+    static constexpr int kOffBar = kOffRing + kSlots * kKVTile;
     static constexpr int kBytes = kOffBar + 256;
-    static constexpr int kTmemCols = (2 * kBN + 2 * HD) <= 256 ? 256 : 512;
-    static constexpr int kColS = 0;                         // + t * kBN
-    static constexpr int kColO = 2 * kBN;                   // + t * HD
+    static constexpr int kTmemCols = 512;
+    static constexpr int kColS = 0;                         // S/P of head t at t * kBN
+    static constexpr int kColO = 2 * kBN;                   // O of head t at kColO + t * HD
+    static_assert(kColO + 2 * HD <= kTmemCols, "tensor memory");
 };
 
 template <int HD>
@@ -308,12 +344,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
     uint64_t *q_full = bars + 0;
-    uint64_t *kv_full = bars + 1;      // [kStages]
-    uint64_t *kv_empty = bars + 4;     // [kStages]
-    uint64_t *s_full = bars + 7;       // [2]
-    uint64_t *s_free = bars + 9;       // [2]
-    uint64_t *p_full = bars + 11;      // [2]
-    uint64_t *o_ready = bars + 13;     // [2]
+    uint64_t *slot_full = bars + 1;    // [kSlots] a K or V tile landed
+    uint64_t *slot_free = bars + 5;    // [kSlots] its MMAs are done with it
+    uint64_t *s_full = bars + 9;       // [2] S of head t in TMEM
+    uint64_t *p_full = bars + 11;      // [2] P of head t in TMEM (4 warp arrivals)
+    uint64_t *o_done = bars + 13;      // [2] P V of head t complete
     uint64_t *drain = bars + 15;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 17);
@@ -328,15 +363,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     }
     if (tid == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&slot_full[s], 1);
+            mbar_init(&slot_free[s], 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s_full[t], 1);
-            mbar_init(&s_free[t], kBM);
-            mbar_init(&p_full[t], kBM);
-            mbar_init(&o_ready[t], 1);
+            mbar_init(&p_full[t], 4);
+            mbar_init(&o_done[t], 1);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -349,7 +383,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------------
-        // TMA producer
+        // TMA producer: Q, then the loads K_0, V_0, K_1, V_1, ... into a
+        // ring of kSlots tiles (load n -> slot n % kSlots)
         // ------------------------------------------------------------------
         if (lane == 0) {
             prefetch_tensormap(&qmap);
@@ -365,21 +400,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             const int TB = p.paged ? (bs < kBN ? bs : kBN) : kBN;
             const int32_t *bt_row = p.paged ? p.bt + (int64_t)seq * p.bt_stride : nullptr;
             int issued = 0;
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % kStages;
-                if (j >= kStages &&
-                    !wait_or_abort(&kv_empty[s], (uint32_t)((j / kStages) - 1) & 1u, abort_flag))
+            for (int n = 0; n < 2 * n_kv; ++n) {
+                const int s = n % kSlots;
+                const int j = n >> 1;
+                const CUtensorMap *map = (n & 1) ? &vmap : &kmap;
+                if (n >= kSlots &&
+                    !wait_or_abort(&slot_free[s], (uint32_t)((n / kSlots) - 1) & 1u, abort_flag))
                     break;
-                unsigned char *kdst = smem + L::kOffKV + s * L::kStage;
-                unsigned char *vdst = kdst + L::kKTile;
+                unsigned char *dst = smem + L::kOffRing + s * L::kKVTile;
                 if (!p.paged) {
-                    mbar_arrive_expect_tx(&kv_full[s], (uint32_t)(2 * L::kKTile));
-                    for (int hf = 0; hf < H; ++hf) {
-                        tma_load_3d(kdst + hf * kBN * 128, &kmap, &kv_full[s], hf * 64, kvh,
+                    mbar_arrive_expect_tx(&slot_full[s], (uint32_t)L::kKVTile);
+                    for (int hf = 0; hf < H; ++hf)
+                        tma_load_3d(dst + hf * kBN * 128, map, &slot_full[s], hf * 64, kvh,
                                     k0 + j * kBN, pol_stream);
-                        tma_load_3d(vdst + hf * kBN * 128, &vmap, &kv_full[s], hf * 64, kvh,
-                                    k0 + j * kBN, pol_stream);
-                    }
                 } else {
                     const int nseg = kBN / TB;
                     int ok = 0;
@@ -390,97 +423,85 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
                         if (blk >= 0 && blk < p.num_blocks) ++ok;
                     }
-                    mbar_arrive_expect_tx(&kv_full[s], (uint32_t)(ok * H * 2 * TB * 128));
+                    mbar_arrive_expect_tx(&slot_full[s], (uint32_t)(ok * H * TB * 128));
                     for (int sg = 0; sg < nseg; ++sg) {
                         const int pos = j * kBN + sg * TB;
                         if (pos >= Lk) break;
                         const int lb = pos / bs;
                         const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
                         if (blk < 0 || blk >= p.num_blocks) {
-                            atomicOr(&g_prefill_status, PKV_STATUS_BAD_BLOCK);
+                            if (!(n & 1)) atomicOr(&g_prefill_status, PKV_STATUS_BAD_BLOCK);
                             continue;
                         }
                         const int z = (int)((int64_t)blk * bs + pos % bs);
-                        for (int hf = 0; hf < H; ++hf) {
-                            const int o = hf * kBN * 128 + sg * TB * 128;
-                            tma_load_3d(kdst + o, &kmap, &kv_full[s], hf * 64, kvh, z, pol_stream);
-                            tma_load_3d(vdst + o, &vmap, &kv_full[s], hf * 64, kvh, z, pol_stream);
-                        }
+                        for (int hf = 0; hf < H; ++hf)
+                            tma_load_3d(dst + hf * kBN * 128 + sg * TB * 128, map, &slot_full[s],
+                                        hf * 64, kvh, z, pol_stream);
                     }
                 }
                 ++issued;
             }
             // no copy may still be landing when the CTA leaves
-            for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
-                (void)mbar_wait(&kv_full[j % kStages], (uint32_t)(j / kStages) & 1u);
+            for (int n = issued - kSlots < 0 ? 0 : issued - kSlots; n < issued; ++n)
+                (void)mbar_wait(&slot_full[n % kSlots], (uint32_t)(n / kSlots) & 1u);
             (void)mbar_wait(q_full, 0);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------
-        // MMA issuer (lane 0); the whole warp zeroes value rows past the
-        // keys of a paged sequence
+        // MMA issuer (lane 0).  Order: S_A(0), S_B(0), then per tile j:
+        // P_A(j) V_j, S_A(j+1), P_B(j) V_j, S_B(j+1) -- the tensor core works
+        // on one head while the other head's softmax runs.  P is read from
+        // tensor memory (it overwrites the head's S columns), V and K/Q from
+        // shared memory.  The whole warp zeroes value rows past the keys of a
+        // paged sequence.
         // ------------------------------------------------------------------
         constexpr uint32_t kIdS = idesc_bf16(kBM, kBN, false);
         constexpr uint32_t kIdO = idesc_bf16(kBM, HD, true);
         const uint32_t sbase = smem_u32(smem);
+        const uint32_t ring = sbase + L::kOffRing;
         auto issue_S = [&](int j, int t) {
-            const uint32_t kb = sbase + L::kOffKV + (j % kStages) * L::kStage;
-            const uint32_t qb = sbase + t * L::kQTile;
+            const int s = (2 * j) % kSlots;
+            const uint64_t a0 = sdesc_sw128(sbase + t * L::kQTile, 16, 1024);
+            const uint64_t b0 = sdesc_sw128(ring + s * L::kKVTile, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
-                const int hf = kk / 4;
-                const uint32_t ko = (kk % 4) * 32;
-                const uint64_t a = sdesc_sw128(qb + hf * kBM * 128 + ko, 16, 1024);
-                const uint64_t b = sdesc_sw128(kb + hf * kBN * 128 + ko, 16, 1024);
-                umma_bf16(tmem + L::kColS + t * kBN, a, b, kIdS, kk > 0 ? 1u : 0u);
+                const uint32_t step = (uint32_t)(((kk / 4) * kBN * 128 + (kk % 4) * 32) >> 4);
+                const uint32_t astep = (uint32_t)(((kk / 4) * kBM * 128 + (kk % 4) * 32) >> 4);
+                umma_bf16(tmem + L::kColS + t * kBN, a0 + astep, b0 + step, kIdS, kk > 0 ? 1u : 0u);
             }
             umma_commit(&s_full[t]);
         };
         auto issue_PV = [&](int j, int t) {
-            const uint32_t vb = sbase + L::kOffKV + (j % kStages) * L::kStage + L::kKTile;
-            const uint32_t pb = sbase + L::kOffP + t * L::kPTile;
+            const int s = (2 * j + 1) % kSlots;
+            const uint64_t b0 = sdesc_sw128(ring + s * L::kKVTile, kBN * 128, 1024);
+            const uint32_t a_tm = tmem + L::kColS + t * kBN;           // P: kBN/2 columns
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-                const uint64_t a = sdesc_sw128(pb + kk * 32, 16, 1024);
-                const uint64_t b = sdesc_sw128(vb + kk * 16 * 128, kBN * 128, 1024);
-                umma_bf16(tmem + L::kColO + t * HD, a, b, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-            }
-            umma_commit(&o_ready[t]);
+            for (int kk = 0; kk < kBN / 16; ++kk)
+                umma_bf16_ts(tmem + L::kColO + t * HD, a_tm + kk * 8, b0 + (uint32_t)((kk * 16 * 128) >> 4),
+                             kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&o_done[t]);
         };
         bool live = true;
         if (lane == 0) {
-            live = wait_or_abort(q_full, 0, abort_flag) && wait_or_abort(&kv_full[0], 0, abort_flag);
+            live = wait_or_abort(q_full, 0, abort_flag) && wait_or_abort(&slot_full[0], 0, abort_flag);
             if (live) {
                 tc_fence_after();
                 for (int t = 0; t < ntile; ++t) issue_S(0, t);
+                umma_commit(&slot_free[0]);
             }
         }
         live = __shfl_sync(0xffffffffu, live ? 1 : 0, 0) != 0;
         for (int j = 0; j < n_kv && live; ++j) {
-            if (lane == 0) {
-                if (j + 1 < n_kv) {
-                    const int s1 = (j + 1) % kStages;
-                    live = wait_or_abort(&kv_full[s1], (uint32_t)((j + 1) / kStages) & 1u, abort_flag);
-                    for (int t = 0; t < ntile && live; ++t) {
-                        live = wait_or_abort(&s_free[t], (uint32_t)j & 1u, abort_flag);
-                        if (live) {
-                            tc_fence_after();
-                            issue_S(j + 1, t);
-                        }
-                    }
-                }
-            }
-            live = __shfl_sync(0xffffffffu, live ? 1 : 0, 0) != 0;
-            if (!live) break;
+            const int nv = 2 * j + 1;                       // load index of V_j
+            const int sv = nv % kSlots;
             if (p.paged && j == n_kv - 1 && (j + 1) * kBN > Lk) {
-                // the tile landed (every lane observes the barrier), then zero rows >= Lk
-                const int s = j % kStages;
-                live = wait_or_abort(&kv_full[s], (uint32_t)(j / kStages) & 1u, abort_flag);
-                if (__shfl_sync(0xffffffffu, live ? 1 : 0, 0) == 0 || !__all_sync(0xffffffffu, live)) {
+                // V_j landed (every lane observes the barrier); zero rows >= Lk
+                live = wait_or_abort(&slot_full[sv], (uint32_t)(nv / kSlots) & 1u, abort_flag);
+                if (!__all_sync(0xffffffffu, live)) {
                     live = false;
                     break;
                 }
-                unsigned char *vt = smem + L::kOffKV + s * L::kStage + L::kKTile;
+                unsigned char *vt = smem + L::kOffRing + sv * L::kKVTile;
                 const int first = Lk - j * kBN;
                 for (int r = first; r < kBN; ++r)
                     for (int hf = 0; hf < H; ++hf)
@@ -489,14 +510,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 __syncwarp();
             }
             if (lane == 0) {
+                const bool next = j + 1 < n_kv;
+                const int nk = 2 * j + 2;                   // load index of K_{j+1}
+                live = wait_or_abort(&slot_full[sv], (uint32_t)(nv / kSlots) & 1u, abort_flag);
                 for (int t = 0; t < ntile && live; ++t) {
                     live = wait_or_abort(&p_full[t], (uint32_t)j & 1u, abort_flag);
-                    if (live) {
-                        tc_fence_after();
-                        issue_PV(j, t);
+                    if (!live) break;
+                    tc_fence_after();
+                    issue_PV(j, t);
+                    if (next) {
+                        if (t == 0)
+                            live = wait_or_abort(&slot_full[nk % kSlots], (uint32_t)(nk / kSlots) & 1u,
+                                                 abort_flag);
+                        if (live) issue_S(j + 1, t);
                     }
                 }
-                if (live) umma_commit(&kv_empty[j % kStages]);
+                if (live) {
+                    umma_commit(&slot_free[sv]);                    // V_j
+                    if (next) umma_commit(&slot_free[nk % kSlots]); // K_{j+1}
+                }
             }
             live = __shfl_sync(0xffffffffu, live ? 1 : 0, 0) != 0;
         }
@@ -517,44 +549,30 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
             const uint32_t tS = tmem + lane_base + L::kColS + t * kBN;
             const uint32_t tO = tmem + lane_base + L::kColO + t * HD;
-            const uint32_t prow = smem_u32(smem + L::kOffP + t * L::kPTile + row * 128);
-            const int sw = row & 7;
+            const float sc = p.scale_log2;
             float m = -INFINITY, l = 0.f;
             bool live = true;
             for (int j = 0; j < n_kv; ++j) {
                 live = wait_or_abort(&s_full[t], (uint32_t)j & 1u, abort_flag);
                 if (!__all_sync(0xffffffffu, live)) { live = false; break; }
                 tc_fence_after();
-                float s[kBN];
-                {
-                    float a[32], b[32];
-                    tmem_ld32(tS, a);
-                    tmem_ld32(tS + 32, b);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        s[c] = a[c];
-                        s[32 + c] = b[c];
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(&s_free[t]);
-                // scale, causal mask, row maximum
+                uint32_t sr[kBN];
+                tmem_ld128(tS, sr);
+                // row maximum of the raw scores (scale > 0), causal mask on the
+                // tiles that cross the row's bound
                 const int limit = off + qi - j * kBN;   // columns <= limit are visible
                 float rmax = -INFINITY;
                 if (limit >= kBN - 1) {
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c) {
-                        s[c] *= p.scale_log2;
-                        rmax = fmaxf(rmax, s[c]);
-                    }
+                    for (int c = 0; c < kBN; ++c) rmax = fmaxf(rmax, __uint_as_float(sr[c]));
                 } else {
 #pragma unroll
                     for (int c = 0; c < kBN; ++c) {
-                        s[c] = c <= limit ? s[c] * p.scale_log2 : -INFINITY;
-                        rmax = fmaxf(rmax, s[c]);
+                        if (c > limit) sr[c] = __float_as_uint(-INFINITY);
+                        rmax = fmaxf(rmax, __uint_as_float(sr[c]));
                     }
                 }
-                const float m_new = fmaxf(m, rmax);
+                const float m_new = fmaxf(m, rmax * sc);
                 const bool rescale = (m == -INFINITY) ? (m_new != -INFINITY)
                                                       : (m_new > m + kRescaleThreshold);
                 float alpha = 1.f;
@@ -563,41 +581,46 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     m = m_new;
                 }
                 const float mu = (m == -INFINITY) ? 0.f : m;
-                l *= alpha;
-                uint32_t pk[kBN / 2];
+                // S_t(j) follows P_t(j-1) V_{j-1} on the tensor core, so O is
+                // final for the earlier tiles: rescale it in place if needed
+                if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                    for (int cc = 0; cc < HD / 32; ++cc) {
+                        float o[32];
+                        tmem_ld32(tO + cc * 32, o);
 #pragma unroll
-                for (int c = 0; c < kBN; c += 2) {
-                    const float e0 = fast_exp2(s[c] - mu);
-                    const float e1 = fast_exp2(s[c + 1] - mu);
-                    l += e0 + e1;
-                    pk[c / 2] = pack_bf16x2(e0, e1);
-                }
-                // P V of the previous tile must be complete: O is stable and the P buffer is free
-                if (j > 0) {
-                    live = wait_or_abort(&o_ready[t], (uint32_t)(j - 1) & 1u, abort_flag);
-                    if (!__all_sync(0xffffffffu, live)) { live = false; break; }
-                    tc_fence_after();
-                    if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-                        for (int cc = 0; cc < HD / 32; ++cc) {
-                            float o[32];
-                            tmem_ld32(tO + cc * 32, o);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                            tmem_st32(tO + cc * 32, o);
-                        }
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(tO + cc * 32, o);
                     }
                 }
+                l *= alpha;
+                // p = 2^(s*scale - m), bf16 pairs written over the S columns
+                const float2 sc2 = make_float2(sc, sc);
+                const float2 nm2 = make_float2(-mu, -mu);
+                float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int c8 = 0; c8 < kBN / 8; ++c8)
-                    st_shared_v4(prow + ((c8 ^ sw) << 4), pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2],
-                                 pk[c8 * 4 + 3]);
-                fence_proxy_async_smem();
+                for (int hpart = 0; hpart < 2; ++hpart) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int col = hpart * 64 + 2 * c;
+                        const float2 x = ffma2(make_float2(__uint_as_float(sr[col]),
+                                                           __uint_as_float(sr[col + 1])), sc2, nm2);
+                        const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        acc = make_float2(acc.x + e.x, acc.y + e.y);
+                        pk[c] = pack_bf16x2(e.x, e.y);
+                    }
+                    tmem_st32_nowait(tS + hpart * 32, pk);
+                }
+                tmem_wait_st();
+                l += acc.x + acc.y;
                 tc_fence_before();
-                mbar_arrive(&p_full[t]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[t]);
             }
             // epilogue: O / l -> bf16 rows, lse
-            if (live) live = wait_or_abort(&o_ready[t], (uint32_t)(n_kv - 1) & 1u, abort_flag);
+            if (live)
+                live = wait_or_abort(&o_done[t], (uint32_t)(n_kv - 1) & 1u, abort_flag);
             if (__all_sync(0xffffffffu, live)) {
                 tc_fence_after();
                 const bool row_ok = qi < Lq;

@@ -339,6 +339,25 @@ def cpu_baseline_decode(work, seconds: float = 10.0, max_rows: int = 64):
 
 
 # ---------------------------------------------------------------------------
+def decode_traffic_from_profile():
+    """DRAM bytes per launch of the decode split kernel from the committed ncu
+    summary, or None when the kernel source changed since it was captured."""
+    import hashlib
+    import re
+    prof = ROOT / "profiles" / "decode_split_qwen3_b64.md"
+    src = ROOT / "paged_kv_cache_303_gb300" / "csrc" / "decode.cu"
+    if not prof.exists() or not src.exists():
+        return None
+    text = prof.read_text()
+    m_hash = re.search(r"sha256 prefix ([0-9a-f]{16})", text)
+    m_bytes = re.search(r"traffic_bytes_per_launch \| (\d+)", text)
+    if not m_hash or not m_bytes:
+        return None
+    if hashlib.sha256(src.read_bytes()).hexdigest()[:16] != m_hash.group(1):
+        return None
+    return int(m_bytes.group(1))
+
+
 def run_ours(args, rank, world):
     from paged_kv_cache_303_gb300 import build, ops, workloads as W
     build.build()
@@ -425,13 +444,7 @@ def run_ours(args, rank, world):
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": sample}
 
-    traffic = None
-    prof = ROOT / "profiles" / "decode_traffic.json"
-    if prof.exists():
-        try:
-            traffic = json.loads(prof.read_text()).get("bytes_per_launch")
-        except ValueError:
-            traffic = None
+    traffic = decode_traffic_from_profile()
     line = {
         "metric": METRIC,
         "value": round(value, 1),

@@ -31,6 +31,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
 // ---------------------------------------------------------------------------
 // Shared-memory addresses, mbarriers, TMA.
@@ -76,10 +77,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread until the phase
+// completes or about `ns` nanoseconds pass, so that waiting threads do not
+// keep issuing shared-memory requests
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Upper bound of a single wait: about 2^31 cycles (roughly a second at the
-// SM clock).  Each try_wait already suspends for a while in hardware, so the
-// loop spins at most a few million times.
+// SM clock).  Each try_wait suspends the thread in hardware for up to
+// kSuspendNs, so the loop runs at most a few thousand times.
 constexpr long long kWaitCycles = 1ll << 31;
+constexpr uint32_t kSuspendNs = 100000;
 
 // Bounded wait on an mbarrier phase.  Returns false when the bound expired;
 // the caller then records PKV_STATUS_TIMEOUT and leaves.
@@ -87,7 +104,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
         if (clock64() - t0 > kWaitCycles) return false;
     }
 }

@@ -74,7 +74,7 @@ namespace {
 
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per KV tile
-constexpr int kSlots = 4;         // ring of K / V tiles (K_j, V_j, K_j+1, ...)
+constexpr int kSlots = 5;         // ring of K / V tiles (K_j, V_j, K_j+1, ...)
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -224,7 +224,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitCycles) {
             *abort_flag = 1;
@@ -344,14 +344,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
     uint64_t *q_full = bars + 0;
-    uint64_t *slot_full = bars + 1;    // [kSlots] a K or V tile landed
-    uint64_t *slot_free = bars + 5;    // [kSlots] its MMAs are done with it
-    uint64_t *s_full = bars + 9;       // [2] S of head t in TMEM
-    uint64_t *p_full = bars + 11;      // [2] P of head t in TMEM (4 warp arrivals)
-    uint64_t *o_done = bars + 13;      // [2] P V of head t complete
-    uint64_t *drain = bars + 15;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 17);
+    uint64_t *slot_full = q_full + 1;          // [kSlots] a K or V tile landed
+    uint64_t *slot_free = slot_full + kSlots;  // [kSlots] its MMAs are done with it
+    uint64_t *s_full = slot_free + kSlots;     // [2] S of head t in TMEM
+    uint64_t *p_full = s_full + 2;             // [2] P of head t in TMEM (4 warp arrivals)
+    uint64_t *o_done = p_full + 2;             // [2] P V of head t complete
+    uint64_t *v_fix = o_done + 2;              // last V tile of a paged sequence cleaned
+    uint64_t *drain = v_fix + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(drain + 2);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -372,6 +373,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(&p_full[t], 4);
             mbar_init(&o_done[t], 1);
         }
+        mbar_init(v_fix, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -386,6 +388,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // TMA producer: Q, then the loads K_0, V_0, K_1, V_1, ... into a
         // ring of kSlots tiles (load n -> slot n % kSlots)
         // ------------------------------------------------------------------
+        bool issued_all = false;
+        int issued_n = 0;
         if (lane == 0) {
             prefetch_tensormap(&qmap);
             prefetch_tensormap(&kmap);
@@ -441,8 +445,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 }
                 ++issued;
             }
+            issued_n = issued;
+            issued_all = issued == 2 * n_kv;
+        }
+        // paged: zero the value rows past the last key of the final tile once it
+        // has landed, so unwritten cache slots never meet a zero probability
+        const bool fix = __shfl_sync(0xffffffffu, issued_all ? 1 : 0, 0) != 0 && p.paged &&
+                         n_kv * kBN > Lk;
+        if (fix) {
+            const int nv = 2 * n_kv - 1;
+            const int sv = nv % kSlots;
+            const bool ok = wait_or_abort(&slot_full[sv], (uint32_t)(nv / kSlots) & 1u, abort_flag);
+            if (__all_sync(0xffffffffu, ok)) {
+                unsigned char *vt = smem + L::kOffRing + sv * L::kKVTile;
+                const int first = Lk - (n_kv - 1) * kBN;
+                for (int r = first; r < kBN; ++r)
+                    for (int hf = 0; hf < H; ++hf)
+                        *reinterpret_cast<uint32_t *>(vt + hf * kBN * 128 + r * 128 + lane * 4) = 0u;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(v_fix);
+            }
+        }
+        if (lane == 0) {
             // no copy may still be landing when the CTA leaves
-            for (int n = issued - kSlots < 0 ? 0 : issued - kSlots; n < issued; ++n)
+            for (int n = issued_n - kSlots < 0 ? 0 : issued_n - kSlots; n < issued_n; ++n)
                 (void)mbar_wait(&slot_full[n % kSlots], (uint32_t)(n / kSlots) & 1u);
             (void)mbar_wait(q_full, 0);
         }
@@ -452,8 +479,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // P_A(j) V_j, S_A(j+1), P_B(j) V_j, S_B(j+1) -- the tensor core works
         // on one head while the other head's softmax runs.  P is read from
         // tensor memory (it overwrites the head's S columns), V and K/Q from
-        // shared memory.  The whole warp zeroes value rows past the keys of a
-        // paged sequence.
+        // shared memory.
         // ------------------------------------------------------------------
         constexpr uint32_t kIdS = idesc_bf16(kBM, kBN, false);
         constexpr uint32_t kIdO = idesc_bf16(kBM, HD, true);
@@ -481,38 +507,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                              kIdO, (j > 0 || kk > 0) ? 1u : 0u);
             umma_commit(&o_done[t]);
         };
-        bool live = true;
         if (lane == 0) {
-            live = wait_or_abort(q_full, 0, abort_flag) && wait_or_abort(&slot_full[0], 0, abort_flag);
+            bool live = wait_or_abort(q_full, 0, abort_flag) && wait_or_abort(&slot_full[0], 0, abort_flag);
             if (live) {
                 tc_fence_after();
                 for (int t = 0; t < ntile; ++t) issue_S(0, t);
                 umma_commit(&slot_free[0]);
             }
-        }
-        live = __shfl_sync(0xffffffffu, live ? 1 : 0, 0) != 0;
-        for (int j = 0; j < n_kv && live; ++j) {
-            const int nv = 2 * j + 1;                       // load index of V_j
-            const int sv = nv % kSlots;
-            if (p.paged && j == n_kv - 1 && (j + 1) * kBN > Lk) {
-                // V_j landed (every lane observes the barrier); zero rows >= Lk
-                live = wait_or_abort(&slot_full[sv], (uint32_t)(nv / kSlots) & 1u, abort_flag);
-                if (!__all_sync(0xffffffffu, live)) {
-                    live = false;
-                    break;
-                }
-                unsigned char *vt = smem + L::kOffRing + sv * L::kKVTile;
-                const int first = Lk - j * kBN;
-                for (int r = first; r < kBN; ++r)
-                    for (int hf = 0; hf < H; ++hf)
-                        *reinterpret_cast<uint32_t *>(vt + hf * kBN * 128 + r * 128 + lane * 4) = 0u;
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            if (lane == 0) {
+            for (int j = 0; j < n_kv && live; ++j) {
+                const int nv = 2 * j + 1;                   // load index of V_j
+                const int sv = nv % kSlots;
                 const bool next = j + 1 < n_kv;
                 const int nk = 2 * j + 2;                   // load index of K_{j+1}
                 live = wait_or_abort(&slot_full[sv], (uint32_t)(nv / kSlots) & 1u, abort_flag);
+                if (live && p.paged && !next && (j + 1) * kBN > Lk)
+                    live = wait_or_abort(v_fix, 0, abort_flag);
                 for (int t = 0; t < ntile && live; ++t) {
                     live = wait_or_abort(&p_full[t], (uint32_t)j & 1u, abort_flag);
                     if (!live) break;
@@ -530,7 +539,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     if (next) umma_commit(&slot_free[nk % kSlots]); // K_{j+1}
                 }
             }
-            live = __shfl_sync(0xffffffffu, live ? 1 : 0, 0) != 0;
         }
         if (lane == 0) {
             // every MMA issued by this thread has completed before TMEM is released
@@ -561,17 +569,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 // row maximum of the raw scores (scale > 0), causal mask on the
                 // tiles that cross the row's bound
                 const int limit = off + qi - j * kBN;   // columns <= limit are visible
-                float rmax = -INFINITY;
-                if (limit >= kBN - 1) {
+                if (limit < kBN - 1) {
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c) rmax = fmaxf(rmax, __uint_as_float(sr[c]));
-                } else {
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c) {
+                    for (int c = 0; c < kBN; ++c)
                         if (c > limit) sr[c] = __float_as_uint(-INFINITY);
-                        rmax = fmaxf(rmax, __uint_as_float(sr[c]));
-                    }
                 }
+                // eight independent partial maxima keep the dependency chains short
+                float pm[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) pm[i] = __uint_as_float(sr[i]);
+#pragma unroll
+                for (int c = 8; c < kBN; ++c) pm[c & 7] = fmaxf(pm[c & 7], __uint_as_float(sr[c]));
+                const float rmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                         fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
                 const float m_new = fmaxf(m, rmax * sc);
                 const bool rescale = (m == -INFINITY) ? (m_new != -INFINITY)
                                                       : (m_new > m + kRescaleThreshold);
@@ -597,7 +607,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 // p = 2^(s*scale - m), bf16 pairs written over the S columns
                 const float2 sc2 = make_float2(sc, sc);
                 const float2 nm2 = make_float2(-mu, -mu);
-                float2 acc = make_float2(0.f, 0.f);
+                float2 acc[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int hpart = 0; hpart < 2; ++hpart) {
                     uint32_t pk[32];
@@ -607,13 +619,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         const float2 x = ffma2(make_float2(__uint_as_float(sr[col]),
                                                            __uint_as_float(sr[col + 1])), sc2, nm2);
                         const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                        acc = make_float2(acc.x + e.x, acc.y + e.y);
+                        acc[c & 3] = fadd2(acc[c & 3], e);
                         pk[c] = pack_bf16x2(e.x, e.y);
                     }
                     tmem_st32_nowait(tS + hpart * 32, pk);
                 }
                 tmem_wait_st();
-                l += acc.x + acc.y;
+                l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                     ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[t]);

@@ -512,8 +512,15 @@ int launch_split(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParam
                  int num_kv_heads, cudaStream_t stream, const char **err) {
     auto kern = decode_split_kernel<HD, G, SW>;
     const size_t smem = 1024 /*alignment slack*/ + Layout<HD, G>::kBytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static bool configured[64];                        // per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
+    if (!configured[dev & 63]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
+        configured[dev & 63] = true;
+    }
     dim3 grid(num_kv_heads, p.max_splits, batch);
     kern<<<grid, kThreads, smem, stream>>>(km, vm, p);
     e = cudaGetLastError();

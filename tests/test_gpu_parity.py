@@ -519,3 +519,41 @@ def test_validate_mode_reports_bad_table():
         assert e.value.code == 5
     finally:
         ops.set_validate(False)
+
+
+def test_decode_step_replayed_as_cuda_graph():
+    """The padded decode step (decode slots, kv_store, decode) captured once
+    in a CUDA graph and replayed on new inputs gives the eager result."""
+    heads = W.Heads(16, 8, 128, 256, 64)
+    work = W.decode_work(heads, [300, 0, 1000, 17], seed=950)
+    kc, vc = W.history_cache(heads, 951)
+    gk, gv = dev(kc), dev(vc)
+    q, k, v = dev(work.q), dev(work.k), dev(work.v)
+    bt, ctx = dev(work.block_tables), dev(work.context_lens)
+    slots = torch.empty(work.batch, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    ws = torch.empty(max(1, ops.decode_workspace_size(work.batch, 16, 8, 128, 1000)),
+                     dtype=torch.uint8, device="cuda")
+
+    def step():
+        ops.kv_build_decode_slots(bt, ctx, 256, out=slots)
+        ops.kv_store(k, v, gk, gv, slots)
+        ops.paged_attn_decode(q, gk, gv, bt, ctx, 1000, heads.scale, out=out, workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    new_q = W.normal_bf16(tuple(q.shape), W.generator(952)).cuda()
+    q.copy_(new_q)
+    graph.replay()
+    torch.cuda.synchronize()
+    got = out.clone()
+    step()
+    torch.cuda.synchronize()
+    assert torch.equal(got, out)
+    assert got[1].eq(0).all()

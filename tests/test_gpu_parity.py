@@ -557,3 +557,39 @@ def test_decode_step_replayed_as_cuda_graph():
     torch.cuda.synchronize()
     assert torch.equal(got, out)
     assert got[1].eq(0).all()
+
+
+def test_mixed_batch_chunks_and_decode_rows_in_one_prefill():
+    """Chunked-prefill mixed batch: sequences with a cached prefix and a new
+    chunk, and decode rows (one new token over their whole cache), run as one
+    paged prefill launch.  A decode row is the Lq = 1 case of the
+    bottom-right causal mask, so it must equal the decode kernel too."""
+    heads = W.Heads(16, 8, 128, 256, 160)
+    q_lens = [200, 1, 77, 1, 1]
+    prefix = [512, 999, 0, 3000, 255]
+    work = W.prefill_work(heads, q_lens, prefix, seed=960)
+    kc, vc = W.history_cache(heads, 961)
+    _poison_unused(kc, vc, work.block_tables, work.prefix_lens)
+    kref, vref = bits(kc).copy(), bits(vc).copy()
+    slots = oracle.slot_mapping(work.block_tables, work.prefix_lens, work.cu_seqlens_q, 256)
+    oracle.kv_store(bits(work.k), bits(work.v), kref, vref, slots)
+    ref, _ = oracle.prefill(bits(work.q), None, None, work.cu_seqlens_q, work.cu_seqlens_k,
+                            heads.scale, k_cache=kref, v_cache=vref, block_tables=work.block_tables)
+    gk, gv = dev(kc), dev(vc)
+    bt = dev(work.block_tables)
+    gs = ops.kv_build_slot_mapping(bt, dev(work.prefix_lens), dev(work.cu_seqlens_q), 256)
+    ops.kv_store(dev(work.k), dev(work.v), gk, gv, gs)
+    out = ops.paged_attn_prefill(dev(work.q), None, None, dev(work.cu_seqlens_q),
+                                 dev(work.cu_seqlens_k), work.max_seqlen_q, work.max_seqlen_k,
+                                 heads.scale, k_cache=gk, v_cache=gv, block_tables=bt)
+    torch.cuda.synchronize()
+    assert_close(out, ref, "mixed batch")
+    # the decode rows through the decode kernel give the same rows
+    cu = work.cu_seqlens_q.tolist()
+    rows = [cu[i] for i in range(len(q_lens)) if q_lens[i] == 1]
+    seqs = [i for i in range(len(q_lens)) if q_lens[i] == 1]
+    ctx = torch.tensor([prefix[i] + 1 for i in seqs], dtype=torch.int32)
+    dec = ops.paged_attn_decode(dev(work.q[rows]), gk, gv, dev(work.block_tables[seqs].contiguous()),
+                                dev(ctx), int(ctx.max()), heads.scale)
+    torch.cuda.synchronize()
+    assert_close(dec, ref[rows], "decode rows of the mixed batch")

@@ -36,7 +36,10 @@ import numpy as np
 
 _DIR = Path(__file__).resolve().parent
 _SRC = _DIR / "oracle.c"
-_LIB = _DIR / "liboracle.so"
+# ORACLE_PLANT names one ORC_PLANT_* macro of oracle.c to compile in (used only
+# by the test that checks the pins catch planted mistakes)
+_PLANT = os.environ.get("ORACLE_PLANT", "")
+_LIB = _DIR / (f"liboracle_{_PLANT.lower()}.so" if _PLANT else "liboracle.so")
 
 ERRORS = {
     -1: "invalid argument",
@@ -59,7 +62,7 @@ def build(force: bool = False) -> Path:
     if force or not _LIB.exists() or _LIB.stat().st_mtime < _SRC.stat().st_mtime:
         tmp = _LIB.with_suffix(f".so.tmp{os.getpid()}")
         cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
-               "-o", str(tmp), str(_SRC), "-lm"]
+               *([f"-D{_PLANT}"] if _PLANT else []), "-o", str(tmp), str(_SRC), "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB

@@ -24,6 +24,10 @@
  *
  * Every function returns 0 on success or a negative ORC_E* code on invalid
  * input; it never reads or writes out of the bounds its arguments describe.
+ *
+ * ORC_PLANT_* macros (never defined in normal builds) each plant one
+ * plausible mistake; tests/test_oracle_planted.py rebuilds the oracle with
+ * each of them and checks that the pins catch it.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -131,8 +135,13 @@ int orc_slot_mapping_per_token(const int32_t *block_tables, int64_t bt_stride,
             int64_t lb = p / block_size;
             if (lb >= max_blocks || row[lb] < 0)
                 return ORC_ETABLE;
+#ifdef ORC_PLANT_SLOT_OFFSET
+            slot_mapping[cu_seqlens_q[i] + t] =
+                (int32_t)((int64_t)row[lb] * block_size + (p + 1) % block_size);
+#else
             slot_mapping[cu_seqlens_q[i] + t] =
                 (int32_t)((int64_t)row[lb] * block_size + p % block_size);
+#endif
         }
     }
     return ORC_OK;
@@ -210,8 +219,13 @@ int orc_kv_store(const uint16_t *key, int64_t key_row_stride,
     free(seen);
     for (int64_t n = 0; n < num_tokens; ++n) {
         int64_t s = slot_mapping[n];
+#ifdef ORC_PLANT_KEEP_PADDING
+        if (s == -1)
+            s = num_slots - 1;
+#else
         if (s == -1)
             continue;
+#endif
         for (int64_t e = 0; e < D; ++e) {
             k_cache[s * D + e] = key[n * key_row_stride + e];
             v_cache[s * D + e] = value[n * value_row_stride + e];
@@ -271,7 +285,11 @@ static int attend_row(const orc_attn_args *a, int32_t i, int64_t k_begin,
                       double *s, double *o, double *lse_out)
 {
     const int32_t g = a->Hq / a->Hkv;
+#ifdef ORC_PLANT_GQA_MODULO
+    const int32_t kvh = h % a->Hkv;
+#else
     const int32_t kvh = h / g;
+#endif
     const uint16_t *qr = a->q + q_row * a->q_rs + (int64_t)h * a->d;
     for (int32_t e = 0; e < a->d; ++e)
         o[e] = 0.0;
@@ -287,7 +305,11 @@ static int attend_row(const orc_attn_args *a, int32_t i, int64_t k_begin,
         double dot = 0.0;
         for (int32_t e = 0; e < a->d; ++e)
             dot += bf16_to_f64(qr[e]) * bf16_to_f64(kr[e]);
+#ifdef ORC_PLANT_NO_SCALE
+        s[j] = dot;
+#else
         s[j] = a->scale * dot;
+#endif
     }
     /* step 2: row softmax, shifted by the row maximum */
     double m = s[0];
@@ -305,8 +327,13 @@ static int attend_row(const orc_attn_args *a, int32_t i, int64_t k_begin,
         if (!vr)
             return ORC_ETABLE;
         double p = s[j] / l;
+#ifdef ORC_PLANT_V_REVERSED
+        for (int32_t e = 0; e < a->d; ++e)
+            o[e] += p * bf16_to_f64(vr[a->d - 1 - e]);
+#else
         for (int32_t e = 0; e < a->d; ++e)
             o[e] += p * bf16_to_f64(vr[e]);
+#endif
     }
     *lse_out = m + log(l);
     return ORC_OK;
@@ -397,7 +424,11 @@ int orc_prefill(const uint16_t *q, int64_t q_rs,
                 for (int64_t t = 0; t < lq; ++t) {
                     int64_t row = cu_seqlens_q[i] + t;
                     double l;
+#ifdef ORC_PLANT_CAUSAL_OFF_BY_ONE
+                    int r = attend_row(&a, i, cu_seqlens_k[i], row, h, lk - lq + t, s, o, &l);
+#else
                     int r = attend_row(&a, i, cu_seqlens_k[i], row, h, lk - lq + t + 1, s, o, &l);
+#endif
                     if (r) {
 #pragma omp atomic write
                         rc = r;
@@ -502,7 +533,11 @@ int orc_online_softmax(const double *s, const double *v, int64_t n, int64_t w,
             if (s[j] > mb)
                 mb = s[j];
         double m_new = mb > m ? mb : m;
+#ifdef ORC_PLANT_NO_RESCALE
+        double f = 1.0;
+#else
         double f = (m == -INFINITY) ? 0.0 : exp(m - m_new);
+#endif
         l *= f;
         for (int64_t e = 0; e < w; ++e)
             acc[e] *= f;

@@ -151,11 +151,14 @@ def kv_bytes(ctx: torch.Tensor, heads) -> int:
 
 
 class DecodeStep:
-    """kv_build_decode_slots -> kv_store -> paged_attn_decode on resident inputs."""
+    """kv_build_decode_slots -> kv_store -> paged_attn_decode on resident
+    inputs, or with fused=True the same step as paged_attn_decode_store (the
+    store and the decode in one launch, plus the chunk merge)."""
 
-    def __init__(self, work, cache_seed: int):
+    def __init__(self, work, cache_seed: int, fused: bool = False):
         from paged_kv_cache_303_gb300 import ops, workloads as W
         self.ops, self.work, h = ops, work, work.heads
+        self.fused = fused
         shape = (h.num_blocks, h.block_size, h.num_kv_heads, h.head_dim)
         self.kc = W.fill_normal_(torch.empty(shape, dtype=torch.bfloat16, device="cuda"), cache_seed)
         self.vc = W.fill_normal_(torch.empty(shape, dtype=torch.bfloat16, device="cuda"), cache_seed + 1)
@@ -171,7 +174,10 @@ class DecodeStep:
         live = int((work.context_lens > 0).sum())
         self.qo_bytes = 2 * live * h.num_heads * h.head_dim * 2
         self.store_bytes = live * h.num_kv_heads * h.head_dim * 2 * 4 + 4 * work.batch
-        self.launches = 4 if ws > 0 else 3
+        if fused:
+            self.launches = 2 if ws > 0 else 1
+        else:
+            self.launches = 4 if ws > 0 else 3
 
     def attention(self):
         h = self.work.heads
@@ -195,6 +201,15 @@ class DecodeStep:
 
     def __call__(self, ev=None):
         h = self.work.heads
+        if self.fused:
+            if ev is not None:
+                ev[0].record()
+            self.ops.paged_attn_decode_store(self.q, self.k, self.v, self.kc, self.vc, self.bt,
+                                             self.ctx, self.max_ctx, h.scale, out=self.out,
+                                             workspace=self.ws)
+            if ev is not None:
+                ev[1].record()
+            return
         self.ops.kv_build_decode_slots(self.bt, self.ctx, h.block_size, out=self.slots)
         self.ops.kv_store(self.k, self.v, self.kc, self.vc, self.slots)
         if ev is not None:
@@ -413,6 +428,28 @@ def run_ours(args, rank, world):
     torch.cuda.empty_cache()
 
     also = {}
+    # the same step with the store fused into the decode launch
+    fz = DecodeStep(W.qwen3_decode(), cache_seed=401, fused=True)
+    for _ in range(3):
+        fz()
+    fgraph = fz.capture()
+    f_tot, _, _ = time_steps(lambda ev=None: fgraph.replay(), args.steps, args.warmup, world,
+                             kernel_events=False)
+    f_eager, f_ms, _ = time_steps(fz, args.steps, args.warmup, world)
+    f_bytes = fz.bytes + fz.qo_bytes + fz.store_bytes
+    also["decode_fused"] = {
+        "workload": "qwen3-decode-b64, step = paged_attn_decode_store (store + decode in one "
+                    "launch) + merge, replayed as one CUDA graph",
+        "gbs": round(fz.bytes * world * args.steps / (f_tot / 1e3) / 1e9, 1),
+        "eager_gbs": round(fz.bytes * world * args.steps / (f_eager / 1e3) / 1e9, 1),
+        "step_ms": round(f_tot / args.steps, 4), "kernel_ms": round(f_ms, 4),
+        "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                     "achieved": round(f_bytes / (f_ms / 1e3) / 1e9, 1),
+                     "frac": round(f_bytes / (f_ms / 1e3) / 1e9 / hbm, 4)},
+        "launches_per_step": fz.launches,
+    }
+    del fz, fgraph
+    torch.cuda.empty_cache()
     # varlen prefill step (packed k/v), 8 prompts of U[128, 4096]
     pre = PrefillStep(W.varlen_prefill(), cache_seed=501)
     tot, pre_ms, st_ms = time_steps(pre, args.steps, args.warmup, world, store_events=True)

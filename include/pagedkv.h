@@ -227,6 +227,41 @@ size_t paged_attn_decode_workspace_size(int32_t batch, int32_t num_heads,
                                         int32_t max_context_len);
 
 /* ------------------------------------------------------------------------
+ * paged_attn_decode_store -- the write-then-attend order of Lesson 04 §4
+ * (store_kvcache, then flash_attn_with_kvcache) and the decode slot of
+ * §4/L17 §5.3, in one launch.
+ *
+ * For every row b with context_lens[b] >= 1 it writes key[b] and value[b]
+ * ([num_kv_heads, head_dim] each) to the decode slot of position
+ * ctx_b - 1,
+ *     slot_b = block_tables[b][(ctx_b-1) / block_size] * block_size
+ *              + (ctx_b-1) % block_size,
+ * and then computes exactly what paged_attn_decode computes over the
+ * context_lens[b] tokens, the new one included.  On return (in stream order)
+ * the caches hold the same bytes that kv_build_decode_slots + kv_store would
+ * have written, and out/lse equal paged_attn_decode's bit for bit.
+ *   key, value  [batch, num_kv_heads, head_dim] bf16, row strides in
+ *               elements (multiples of 8; 16-byte aligned pointers).
+ *   k_cache, v_cache are written (only the batch slots above).
+ * Padding rows (context_lens[b] == 0) write nothing.  A block-table entry
+ * outside [0, num_blocks) at the new position skips the write and sets
+ * PKV_STATUS_BAD_BLOCK.  Two rows whose new positions map to the same slot
+ * race (invalid input).  All other arguments, the workspace and the
+ * supported shapes are those of paged_attn_decode.
+ * ---------------------------------------------------------------------- */
+int paged_attn_decode_store(const pkv_bf16 *q, int64_t q_row_stride,
+                            const pkv_bf16 *key, int64_t key_row_stride,
+                            const pkv_bf16 *value, int64_t value_row_stride,
+                            pkv_bf16 *k_cache, pkv_bf16 *v_cache, int64_t num_blocks,
+                            const int32_t *block_tables, int64_t bt_stride,
+                            int32_t max_blocks_per_seq, const int32_t *context_lens,
+                            int32_t batch, int32_t num_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, int32_t max_context_len,
+                            float softmax_scale, pkv_bf16 *out, int64_t out_row_stride,
+                            float *lse, void *workspace, size_t workspace_bytes,
+                            pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * paged_attn_decode_noalloc -- the pages have no counterpart: this entry
  * point exists for callers of this library that cannot allocate device
  * memory, such as a plugin inside a host framework that owns every device

@@ -225,14 +225,20 @@ static int check_heads(const char *what, int32_t num_heads, int32_t num_kv_heads
     return PKV_OK;
 }
 
-int paged_attn_decode(const pkv_bf16 *q, int64_t q_row_stride, const pkv_bf16 *k_cache,
-                      const pkv_bf16 *v_cache, int64_t num_blocks, const int32_t *block_tables,
-                      int64_t bt_stride, int32_t max_blocks_per_seq, const int32_t *context_lens,
-                      int32_t batch, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                      int32_t block_size, int32_t max_context_len, float softmax_scale,
-                      pkv_bf16 *out, int64_t out_row_stride, float *lse, void *workspace,
-                      size_t workspace_bytes, pkv_stream_t stream) {
-    const char *what = "paged_attn_decode";
+}  // extern "C"
+
+// shared by paged_attn_decode and paged_attn_decode_store (key == NULL: the
+// caches are only read)
+static int decode_entry(const char *what, const pkv_bf16 *q, int64_t q_row_stride,
+                        const pkv_bf16 *key, int64_t key_row_stride, const pkv_bf16 *value,
+                        int64_t value_row_stride, const pkv_bf16 *k_cache,
+                        const pkv_bf16 *v_cache, int64_t num_blocks, const int32_t *block_tables,
+                        int64_t bt_stride, int32_t max_blocks_per_seq,
+                        const int32_t *context_lens, int32_t batch, int32_t num_heads,
+                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                        int32_t max_context_len, float softmax_scale, pkv_bf16 *out,
+                        int64_t out_row_stride, float *lse, void *workspace,
+                        size_t workspace_bytes, pkv_stream_t stream) {
     if (int rc = check_heads(what, num_heads, num_kv_heads, head_dim, block_size)) return rc;
     if (batch < 0 || max_context_len < 0 || num_blocks < 0 || max_blocks_per_seq < 0 ||
         bt_stride < max_blocks_per_seq)
@@ -258,6 +264,18 @@ int paged_attn_decode(const pkv_bf16 *q, int64_t q_row_stride, const pkv_bf16 *k
                     what, max_context_len);
     if (num_blocks * block_size > INT32_MAX)
         return fail(PKV_ERR_UNSUPPORTED, "%s: more than 2^31 slots per cache", what);
+    if (key || value) {
+        const int64_t kv_row = (int64_t)num_kv_heads * head_dim;
+        if (!key || !value)
+            return fail(PKV_ERR_INVALID_ARG, "%s: null key or value", what);
+        if (key_row_stride < kv_row || value_row_stride < kv_row)
+            return fail(PKV_ERR_INVALID_ARG,
+                        "%s: key/value row strides below num_kv_heads*head_dim", what);
+        if (key_row_stride % 8 || value_row_stride % 8 || !aligned16(key) || !aligned16(value))
+            return fail(PKV_ERR_UNSUPPORTED,
+                        "%s: key/value must be 16-byte aligned with row strides a multiple of 8",
+                        what);
+    }
     pkv::DecodeArgs a{};
     a.q = q;
     a.q_rs = q_row_stride;
@@ -280,11 +298,49 @@ int paged_attn_decode(const pkv_bf16 *q, int64_t q_row_stride, const pkv_bf16 *k
     a.lse = lse;
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
+    a.new_k = key;
+    a.new_v = value;
+    a.new_k_rs = key_row_stride;
+    a.new_v_rs = value_row_stride;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const char *err = "";
     int rc = pkv::launch_decode(a, s, &err);
     if (rc) return fail(rc, "%s: %s", what, err);
     return post_launch(s, what);
+}
+
+extern "C" {
+
+int paged_attn_decode(const pkv_bf16 *q, int64_t q_row_stride, const pkv_bf16 *k_cache,
+                      const pkv_bf16 *v_cache, int64_t num_blocks, const int32_t *block_tables,
+                      int64_t bt_stride, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                      int32_t batch, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t max_context_len, float softmax_scale,
+                      pkv_bf16 *out, int64_t out_row_stride, float *lse, void *workspace,
+                      size_t workspace_bytes, pkv_stream_t stream) {
+    return decode_entry("paged_attn_decode", q, q_row_stride, nullptr, 0, nullptr, 0, k_cache,
+                        v_cache, num_blocks, block_tables, bt_stride, max_blocks_per_seq,
+                        context_lens, batch, num_heads, num_kv_heads, head_dim, block_size,
+                        max_context_len, softmax_scale, out, out_row_stride, lse, workspace,
+                        workspace_bytes, stream);
+}
+
+int paged_attn_decode_store(const pkv_bf16 *q, int64_t q_row_stride, const pkv_bf16 *key,
+                            int64_t key_row_stride, const pkv_bf16 *value,
+                            int64_t value_row_stride, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                            int64_t num_blocks, const int32_t *block_tables, int64_t bt_stride,
+                            int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
+                            int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t max_context_len, float softmax_scale,
+                            pkv_bf16 *out, int64_t out_row_stride, float *lse, void *workspace,
+                            size_t workspace_bytes, pkv_stream_t stream) {
+    if (batch > 0 && (!key || !value))
+        return fail(PKV_ERR_INVALID_ARG, "paged_attn_decode_store: null key or value");
+    return decode_entry("paged_attn_decode_store", q, q_row_stride, key, key_row_stride, value,
+                        value_row_stride, k_cache, v_cache, num_blocks, block_tables, bt_stride,
+                        max_blocks_per_seq, context_lens, batch, num_heads, num_kv_heads, head_dim,
+                        block_size, max_context_len, softmax_scale, out, out_row_stride, lse,
+                        workspace, workspace_bytes, stream);
 }
 
 size_t paged_attn_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,

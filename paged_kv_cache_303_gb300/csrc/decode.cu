@@ -27,6 +27,13 @@
 //     not complete (sequence tail, missing block) tokens whose probabilities
 //     are all zero are skipped, so garbage in unwritten cache slots never
 //     reaches the sum.
+//   * Fused store (paged_attn_decode_store): the CTA whose chunk holds
+//     position ctx-1 first writes the step's new K/V row of its kv head to
+//     that slot (the decode slot of Lesson 04 §4), with generic stores from
+//     the producer warp, then orders them before its TMA reads with a proxy
+//     fence; the tile that holds the new token then loads it like any other.
+//     Exactly one CTA per (sequence, kv head) writes; a padding row writes
+//     nothing.
 //   * The consumer warps' (m, l, o) are merged once per chunk; a
 //     single-chunk launch writes bf16 out and lse directly, otherwise each CTA
 //     writes (m, l, unnormalised o) in fp32 to the workspace and
@@ -95,6 +102,10 @@ struct DecodeParams {
     float *lse;
     float *part_o;             // [B, Hq, S, HD] fp32 (split mode)
     float *part_ml;            // [B, Hq, S, 2]  fp32 (split mode)
+    // fused store: this step's key/value rows [B, Hkv, HD] (null: no store)
+    const uint16_t *new_k, *new_v;
+    int64_t new_k_rs, new_v_rs;
+    uint16_t *k_cache, *v_cache;
 };
 
 template <int HD, int G>
@@ -171,7 +182,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     const bool direct = (p.max_splits == 1);
 
     int ctx = p.ctx[b];
-    if (ctx < 0 || ctx > p.max_context_len) {
+    const bool ctx_ok = ctx >= 0 && ctx <= p.max_context_len;
+    if (!ctx_ok) {
         if (tid == 0 && split == 0) atomicOr(&g_decode_status, PKV_STATUS_BAD_LENGTH);
         ctx = ctx < 0 ? 0 : p.max_context_len;
     }
@@ -235,6 +247,33 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     const int prologue = ntiles < kStages ? ntiles : kStages;
 
     if (warp == kConsumers) {
+        // fused store: the chunk that holds position ctx-1 writes the new
+        // token's row of this kv head before any tile is requested
+        if (p.new_k != nullptr && ctx_ok && ctx - 1 >= tok_begin && ctx - 1 < tok_end) {
+            const int pos = ctx - 1;
+            const int lb = pos / bs;
+            const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
+            if (blk >= 0 && blk < p.num_blocks) {
+                const int64_t dst = ((int64_t)blk * bs + pos % bs) * p.num_kv_heads * HD +
+                                    (int64_t)kvh * HD + lane * DPL;
+                const uint16_t *ks = p.new_k + (int64_t)b * p.new_k_rs + (int64_t)kvh * HD + lane * DPL;
+                const uint16_t *vs = p.new_v + (int64_t)b * p.new_v_rs + (int64_t)kvh * HD + lane * DPL;
+                if constexpr (DPL == 4) {
+                    const uint2 kw = *reinterpret_cast<const uint2 *>(ks);
+                    const uint2 vw = *reinterpret_cast<const uint2 *>(vs);
+                    *reinterpret_cast<uint2 *>(p.k_cache + dst) = kw;
+                    *reinterpret_cast<uint2 *>(p.v_cache + dst) = vw;
+                } else {
+                    const uint32_t kw = *reinterpret_cast<const uint32_t *>(ks);
+                    const uint32_t vw = *reinterpret_cast<const uint32_t *>(vs);
+                    *reinterpret_cast<uint32_t *>(p.k_cache + dst) = kw;
+                    *reinterpret_cast<uint32_t *>(p.v_cache + dst) = vw;
+                }
+                // the row is read back below by TMA (the async proxy)
+                fence_proxy_async_global();
+            }
+            __syncwarp();
+        }
         // the producer starts the first kStages tiles before anything else,
         // so that their latency overlaps the query load below
         if (lane == 0) {
@@ -595,6 +634,12 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream, const char **err) {
     p.out = a.out;
     p.out_rs = a.out_rs;
     p.lse = a.lse;
+    p.new_k = a.new_k;
+    p.new_v = a.new_v;
+    p.new_k_rs = a.new_k_rs;
+    p.new_v_rs = a.new_v_rs;
+    p.k_cache = const_cast<uint16_t *>(a.k_cache);
+    p.v_cache = const_cast<uint16_t *>(a.v_cache);
     if (splits > 1) {
         const size_t need = decode_workspace_bytes(a.batch, a.num_heads, a.num_kv_heads,
                                                    a.head_dim, a.max_context_len);

@@ -47,6 +47,10 @@ struct DecodeArgs {
     float *lse;
     void *workspace;
     size_t workspace_bytes;
+    // fused store of the step's new token (paged_attn_decode_store); null
+    // new_k means the caches are only read
+    const uint16_t *new_k, *new_v;
+    int64_t new_k_rs, new_v_rs;
 };
 // chunk of keys per split and number of splits for a decode launch
 void decode_plan(int32_t batch, int32_t num_kv_heads, int32_t head_dim, int32_t max_context_len,

@@ -51,6 +51,9 @@ SIGNATURES = {
     "paged_attn_prefill_workspace_size": ([_I32, _I32, _I32, _I32], _SZ),
     "paged_attn_decode": ([_P, _I64, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32, _I32, _I32,
                            _I32, _I32, _F32, _P, _I64, _P, _P, _SZ, _P], _INT),
+    "paged_attn_decode_store": ([_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _I32, _P,
+                                 _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _I64, _P, _P, _SZ,
+                                 _P], _INT),
     "paged_attn_decode_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
     "paged_attn_decode_noalloc": ([_P, _I64, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32, _I32,
                                    _I32, _I32, _I32, _F32, _P, _I64, _P, _P], _INT),
@@ -235,6 +238,42 @@ def paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, max_conte
                                    _ptr(block_tables), bt_stride, width, _ptr(ctx), b, hq, hkv, d, bs,
                                    max_context_len, float(scale), _ptr(out), ors, _ptr(lse),
                                    _ptr(workspace), wbytes, _stream(q.device)))
+    return (out, lse) if return_lse else out
+
+
+def paged_attn_decode_store(q, key, value, k_cache, v_cache, block_tables, context_lens,
+                            max_context_len: int, softmax_scale: Optional[float] = None,
+                            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None, return_lse: bool = False):
+    """Writes this step's key/value [B, Hkv, d] to each row's decode slot and
+    attends over the context (new token included) in one launch."""
+    qrs = _rows(q, "q")
+    krs, vrs = _rows(key, "key"), _rows(value, "value")
+    b, hq, d = q.shape
+    _cuda(k_cache, torch.bfloat16, "k_cache")
+    _cuda(v_cache, torch.bfloat16, "v_cache")
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shape mismatch")
+    if tuple(key.shape) != (b, hkv, d) or tuple(value.shape) != (b, hkv, d):
+        raise ValueError("key/value must be [batch, num_kv_heads, head_dim]")
+    bt_stride, width = _table(block_tables)
+    ctx = _i32(context_lens, "context_lens")
+    scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=q.device)
+    ors = _rows(out, "out")
+    if return_lse and lse is None:
+        lse = torch.empty((b, hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _cuda(lse, torch.float32, "lse")
+    need = decode_workspace_size(b, hq, hkv, d, max_context_len)
+    workspace, wbytes = _workspace(need, q.device, workspace)
+    _check(lib().paged_attn_decode_store(_ptr(q), qrs, _ptr(key), krs, _ptr(value), vrs,
+                                         _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
+                                         bt_stride, width, _ptr(ctx), b, hq, hkv, d, bs,
+                                         max_context_len, float(scale), _ptr(out), ors, _ptr(lse),
+                                         _ptr(workspace), wbytes, _stream(q.device)))
     return (out, lse) if return_lse else out
 
 

@@ -98,6 +98,9 @@ def _load():
                                   _INT], _INT),
             "orc_decode_split": ([_P, _I64, _P, _P, _I64, _P, _I64, _I32, _P, _I32,
                                   _I32, _I32, _I32, _I32, _D, _I64, _P, _P], _INT),
+            "orc_round_bf16": ([_D], ctypes.c_uint16),
+            "orc_qk_norm_rope": ([_P, _I64, _P, _I64, _P, _P, _P, _D, _D, _I64, _I32, _I32,
+                                  _I32, _P, _P], _INT),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -319,3 +322,34 @@ def online_softmax(s, v, block):
     _check(_load().orc_online_softmax(_ptr(s), _ptr(v), n, w, block, _ptr(out), _ptr(m), _ptr(l),
                                       _ptr(trace)), "online_softmax")
     return out, float(m[0]), float(l[0]), trace
+
+
+def round_bf16(x: float) -> int:
+    """Nearest bf16 (ties to even) of a double, as its bit pattern."""
+    return int(_load().orc_round_bf16(float(x)))
+
+
+def qk_norm_rope(q, k, positions, q_weight, k_weight, eps=1e-6, theta=1e6):
+    """QK-Norm then RoPE.  q: uint16 [N, Hq, d], k: uint16 [N, Hkv, d] (rows
+    may be strided, heads contiguous), positions [N] int, weights uint16 [d].
+    Returns (q_out, k_out) as contiguous uint16 arrays of the same shapes."""
+    q, k = _u16(q), _u16(k)
+    n, hq, d = q.shape
+    hkv = k.shape[1]
+    item = q.itemsize
+    for t in (q, k):
+        if t.strides[2] != item or t.strides[1] != d * item or t.shape[0] != n or t.shape[2] != d:
+            raise ValueError("q/k must be [N, heads, d] with heads and d contiguous")
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+    qw = np.ascontiguousarray(_u16(q_weight))
+    kw = np.ascontiguousarray(_u16(k_weight))
+    if pos.size != n or qw.size != d or kw.size != d:
+        raise ValueError("positions must have N entries, weights d entries")
+    qo = np.empty((n, hq, d), np.uint16)
+    ko = np.empty((n, hkv, d), np.uint16)
+    q_rs = q.strides[0] // item if n > 1 else hq * d
+    k_rs = k.strides[0] // item if n > 1 else hkv * d
+    _check(_load().orc_qk_norm_rope(_ptr(q), q_rs, _ptr(k), k_rs, _ptr(pos), _ptr(qw), _ptr(kw),
+                                    float(eps), float(theta), n, hq, hkv, d, _ptr(qo), _ptr(ko)),
+           "qk_norm_rope")
+    return qo, ko

@@ -15,6 +15,11 @@
  *   [P3] "Lesson 04: where exactly does the KV go" (diomchen.github.io)
  *        §2 how slot_mapping is built, §3 the write kernel, §4 two
  *        FlashAttention calls, §7 Exercise A, §9 code hunt item 1.
+ *   [P1] "Nano-VLLM full-code notes (5): layernorm & attention"
+ *        (m.demingchina.com), the RMSNorm module (layernorm.py).
+ *   [RoFormer] Su et al., "RoFormer: Enhanced Transformer with Rotary
+ *        Position Embedding" (2021), the rotary position embedding that
+ *        [P2] §4 applies after QK-Norm but does not print.
  *
  * Arithmetic: bf16 inputs are widened exactly (bits << 16) to float and then
  * to double; every score, exponential, sum and output is computed in double
@@ -750,4 +755,125 @@ int orc_prefill_rows(const uint16_t *q, int64_t q_rs,
         free(o);
     }
     return rc;
+}
+
+/* ------------------------------------------------------------------------
+ * Round a double to the nearest bf16 (ties to even), returned as its bit
+ * pattern.  bf16 keeps 8 significant bits: for |x| = m * 2^k with m in
+ * [0.5, 1), x is rounded to a multiple of 2^(k-8).  Values here are far
+ * from the bf16 overflow and subnormal ranges; those, NaN and infinities go
+ * through float, whose rounding there is the same.
+ * ---------------------------------------------------------------------- */
+uint16_t orc_round_bf16(double x)
+{
+    double ax = fabs(x);
+    uint32_t u;
+    float f;
+    if (ax >= 0x1p-126 && ax < 0x1p127) {
+        int k;
+        double m = frexp(x, &k);      /* x = m * 2^k, 0.5 <= |m| < 1 */
+#ifdef ORC_PLANT_ROUND_TRUNC
+        f = (float)ldexp(trunc(ldexp(m, 8)), k - 8);
+#else
+        f = (float)ldexp(nearbyint(ldexp(m, 8)), k - 8);   /* exact in float */
+#endif
+        memcpy(&u, &f, sizeof u);
+        return (uint16_t)(u >> 16);
+    }
+    /* zero, subnormal range, huge, inf, NaN: through float */
+    f = (float)x;
+    memcpy(&u, &f, sizeof u);
+    if (f != f)
+        return (uint16_t)((u >> 16) | 0x40u);
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------------------------------
+ * QK-Norm then RoPE on one row of head_dim elements ([P2] §4: q and k of
+ * every head are RMS-normalised over head_dim, then rotated by position; v
+ * is left alone).
+ *
+ * RMSNorm ([P1], layernorm.py): widen to float, divide by
+ * sqrt(mean(x^2) + eps), convert back to the input dtype (bf16), and only
+ * then multiply by the bf16 weight (a bf16 product, rounded).  The oracle
+ * keeps the two roundings to bf16 where the module has them and computes
+ * everything else in double.
+ *
+ * RoPE ([RoFormer] §3.2, "rotate-half" pairing): element e < d/2 pairs
+ * with e + d/2; pair i turns by the angle pos * theta^(-2i/d):
+ *     y[i]       = x[i] cos(a_i) - x[i + d/2] sin(a_i)
+ *     y[i + d/2] = x[i + d/2] cos(a_i) + x[i] sin(a_i)
+ * computed in double from the bf16 QK-Norm output and rounded to bf16 once.
+ * ---------------------------------------------------------------------- */
+static void norm_rope_row(const uint16_t *x, const uint16_t *w, int32_t d, double eps,
+                          double pos, double theta, uint16_t *out, double *tmp)
+{
+    double ss = 0.0;
+    for (int32_t e = 0; e < d; ++e) {
+        double v = bf16_to_f64(x[e]);
+        ss += v * v;
+    }
+#if defined(ORC_PLANT_NORM_SUM)
+    double inv = 1.0 / sqrt(ss + eps);
+#elif defined(ORC_PLANT_EPS_OUTSIDE)
+    double inv = 1.0 / (sqrt(ss / d) + eps);
+#else
+    double inv = 1.0 / sqrt(ss / d + eps);
+#endif
+    for (int32_t e = 0; e < d; ++e) {
+        double n = bf16_to_f64(orc_round_bf16(bf16_to_f64(x[e]) * inv));
+        tmp[e] = bf16_to_f64(orc_round_bf16(n * bf16_to_f64(w[e])));
+    }
+    int32_t h = d / 2;
+#ifdef ORC_PLANT_ROPE_INTERLEAVED
+    for (int32_t i = 0; i < h; ++i) {
+        double a = pos * pow(theta, -2.0 * i / d);
+        double c = cos(a), sn = sin(a);
+        out[2 * i] = orc_round_bf16(tmp[2 * i] * c - tmp[2 * i + 1] * sn);
+        out[2 * i + 1] = orc_round_bf16(tmp[2 * i + 1] * c + tmp[2 * i] * sn);
+    }
+    return;
+#endif
+    for (int32_t i = 0; i < h; ++i) {
+#ifdef ORC_PLANT_ROPE_FREQ
+        double a = pos * pow(theta, -1.0 * i / d);
+#else
+        double a = pos * pow(theta, -2.0 * i / d);
+#endif
+        double c = cos(a), sn = sin(a);
+#ifdef ORC_PLANT_ROPE_SIGN
+        sn = -sn;
+#endif
+        out[i] = orc_round_bf16(tmp[i] * c - tmp[i + h] * sn);
+        out[i + h] = orc_round_bf16(tmp[i + h] * c + tmp[i] * sn);
+    }
+}
+
+/* q [N, Hq, d] and k [N, Hkv, d] (bf16 bits, row strides q_rs / k_rs in
+ * elements, heads contiguous) -> q_out [N, Hq, d], k_out [N, Hkv, d]
+ * (contiguous).  positions[n] is token n's absolute position; q_w and k_w
+ * are the d-element bf16 weights of the two norms. */
+int orc_qk_norm_rope(const uint16_t *q, int64_t q_rs, const uint16_t *k, int64_t k_rs,
+                     const int64_t *positions, const uint16_t *q_w, const uint16_t *k_w,
+                     double eps, double theta, int64_t num_tokens, int32_t Hq, int32_t Hkv,
+                     int32_t d, uint16_t *q_out, uint16_t *k_out)
+{
+    if (num_tokens < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d & 1) || eps < 0 || theta <= 0 ||
+        q_rs < (int64_t)Hq * d || k_rs < (int64_t)Hkv * d)
+        return ORC_EARG;
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!tmp)
+        return ORC_ENOMEM;
+    for (int64_t n = 0; n < num_tokens; ++n) {
+        double pos = (double)positions[n];
+        for (int32_t h = 0; h < Hq; ++h)
+            norm_rope_row(q + n * q_rs + (int64_t)h * d, q_w, d, eps, pos, theta,
+                          q_out + (n * Hq + h) * d, tmp);
+        for (int32_t h = 0; h < Hkv; ++h)
+            norm_rope_row(k + n * k_rs + (int64_t)h * d, k_w, d, eps, pos, theta,
+                          k_out + (n * Hkv + h) * d, tmp);
+    }
+    free(tmp);
+    return ORC_OK;
 }

@@ -462,3 +462,132 @@ def test_prefill_rows_equal_full_prefill_rows():
     part, part_lse = oracle.prefill_rows(bits(work.q), None, None, work.cu_seqlens_q,
                                          work.cu_seqlens_k, heads.scale, rows, **kw)
     assert np.array_equal(part, full[rows]) and np.array_equal(part_lse, full_lse[rows])
+
+
+# ---------------------------------------------------------------------------
+# QK-Norm + RoPE prologue (L17 §4; RMSNorm module of "Nano-VLLM full-code
+# notes (5)"; rotary embedding of RoFormer §3.2)
+# ---------------------------------------------------------------------------
+def _bf16_bits(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16) \
+        .numpy().view(np.uint16)
+
+
+def _ones(d):
+    return _bf16_bits(np.ones(d))
+
+
+def test_round_bf16_matches_library_and_breaks_ties_to_even():
+    rng = np.random.default_rng(11)
+    x = np.concatenate([rng.standard_normal(20000), rng.standard_normal(2000) * 1e-30,
+                        rng.standard_normal(2000) * 1e30]).astype(np.float32)
+    lib = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    mine = np.array([oracle.round_bf16(float(v)) for v in x], np.uint16)
+    assert np.array_equal(lib, mine)
+    one = 0x3F80
+    assert oracle.round_bf16(1 + 2.0 ** -8) == one               # tie -> even (1.0)
+    assert oracle.round_bf16(1 + 3 * 2.0 ** -8) == one + 2       # tie -> even (1 + 2^-6)
+    assert oracle.round_bf16(1 + 2.0 ** -8 + 2.0 ** -40) == one + 1   # just above the tie
+
+
+def _prologue(rows, pos, w=None, eps=1e-6, theta=1e6):
+    """rows: float array [n, d] (bf16-exact) used as one q head per token."""
+    rows = np.asarray(rows, np.float64)
+    n, d = rows.shape
+    q = _bf16_bits(rows).reshape(n, 1, d)
+    k = q.copy()
+    w = _ones(d) if w is None else w
+    qo, ko = oracle.qk_norm_rope(q, k, np.broadcast_to(np.asarray(pos, np.int64), (n,)), w, w,
+                                 eps, theta)
+    assert np.array_equal(qo, ko)
+    return f64(qo.reshape(n, d))
+
+
+def test_rmsnorm_of_a_constant_row():
+    # every element equal: x / sqrt(mean(x^2) + eps) = sign(x) / sqrt(1 + eps/x^2)
+    out = _prologue([[0.5] * 64, [3.0] * 64, [-2.0] * 64], 0)
+    assert np.array_equal(out, np.array([[1.0] * 64, [1.0] * 64, [-1.0] * 64]))
+    # eps sits inside the square root: x = 1e-3, eps = 1e-6 -> 1/sqrt(2)
+    x = float(torch.tensor(1e-3).to(torch.bfloat16))
+    out = _prologue([[x] * 64], 0, eps=x * x)
+    assert np.all(out == float(torch.tensor(2 ** -0.5).to(torch.bfloat16)))
+
+
+def test_rmsnorm_output_has_unit_rms_and_ignores_scale():
+    rng = np.random.default_rng(12)
+    rows = f64(_bf16_bits(rng.standard_normal((16, 128)) * 3))
+    out = _prologue(rows, 0)
+    assert np.allclose(np.sqrt((out ** 2).mean(axis=1)), 1.0, atol=2e-3)
+    # with eps = 0, scaling a row by a power of two changes nothing
+    a = _prologue(rows, 0, eps=0.0)
+    b = _prologue(rows * 8.0, 0, eps=0.0)
+    assert np.array_equal(a, b)
+
+
+def test_rmsnorm_weight_scales_each_element():
+    rng = np.random.default_rng(13)
+    rows = f64(_bf16_bits(rng.standard_normal((4, 128))))
+    base = _prologue(rows, 0)
+    assert np.array_equal(_prologue(rows, 0, w=_bf16_bits(np.full(128, 2.0))), 2 * base)
+    w = np.ones(128)
+    w[37] = 0.0
+    w[100] = -1.0
+    got = _prologue(rows, 0, w=_bf16_bits(w))
+    assert np.all(got[:, 37] == 0) and np.array_equal(got[:, 100], -base[:, 100])
+    keep = [e for e in range(128) if e not in (37, 100)]
+    assert np.array_equal(got[:, keep], base[:, keep])
+
+
+@pytest.mark.parametrize("d,theta", [(128, 1e6), (128, 1e4), (64, 1e4)])
+def test_rope_turns_pairs_by_closed_form_angles(d, theta):
+    """Pair i = (e, e + d/2) is the complex number x_e + j x_{e+d/2}, turned by
+    pos * theta^(-2i/d): pair 0 by pos radians, pair d/4 by pos / sqrt(theta)."""
+    rng = np.random.default_rng(14)
+    rows = f64(_bf16_bits(rng.standard_normal((8, d))))
+    base = _prologue(rows, 0, theta=theta)                 # position 0: no rotation
+    h = d // 2
+    for pos in (1, 7, 300, 4095, 32767):
+        out = _prologue(rows, pos, theta=theta)
+        for i, angle in ((0, pos), (d // 4, pos / math.sqrt(theta))):
+            z = (base[:, i] + 1j * base[:, i + h]) * np.exp(1j * angle)
+            tol = 2.0 ** -7 * np.abs(z) + 1e-6
+            assert np.all(np.abs(out[:, i] - z.real) <= tol), (pos, i)
+            assert np.all(np.abs(out[:, i + h] - z.imag) <= tol), (pos, i)
+
+
+def test_rope_keeps_pair_norms_and_depends_on_relative_position():
+    rng = np.random.default_rng(15)
+    d = 128
+    rows = f64(_bf16_bits(rng.standard_normal((2, d))))
+    base = _prologue(rows, 0)
+    out = _prologue(rows, 1234)
+    nb = base[:, :64] ** 2 + base[:, 64:] ** 2
+    no = out[:, :64] ** 2 + out[:, 64:] ** 2
+    assert np.allclose(no, nb, rtol=2e-2, atol=1e-3)
+    # <R(p) q, R(p') k> depends on p - p' only
+    def dot(p, pk):
+        return float((_prologue(rows[:1], p) * _prologue(rows[1:], pk)).sum())
+    for p, pk, s in ((10, 3, 500), (4000, 100, -50), (7, 7, 31000)):
+        assert abs(dot(p, pk) - dot(p + s, pk + s)) <= 0.05 * (1 + abs(dot(p, pk)))
+
+
+def test_prologue_reads_each_tokens_position_and_strided_rows():
+    rng = np.random.default_rng(16)
+    n, hq, hkv, d = 5, 4, 2, 64
+    big = _bf16_bits(rng.standard_normal((n, hq + 2 * hkv, d)))      # fused qkv rows
+    q, k = big[:, :hq], big[:, hq:hq + hkv]
+    pos = [0, 9, 9, 100, 3]
+    qw, kw = _bf16_bits(rng.uniform(0.5, 1.5, d)), _bf16_bits(rng.uniform(0.5, 1.5, d))
+    qo, ko = oracle.qk_norm_rope(q, k, pos, qw, kw)
+    qc, kc = oracle.qk_norm_rope(np.ascontiguousarray(q), np.ascontiguousarray(k), pos, qw, kw)
+    assert np.array_equal(qo, qc) and np.array_equal(ko, kc)
+    for t in range(n):                      # token by token gives the same rows
+        a, b = oracle.qk_norm_rope(q[t:t + 1], k[t:t + 1], pos[t:t + 1], qw, kw)
+        assert np.array_equal(a[0], qo[t]) and np.array_equal(b[0], ko[t])
+    # the two tokens at position 9 differ only through their inputs: swap them
+    q2, k2 = q[[0, 2, 1, 3, 4]], k[[0, 2, 1, 3, 4]]
+    a, b = oracle.qk_norm_rope(q2, k2, pos, qw, kw)
+    assert np.array_equal(a[[0, 2, 1, 3, 4]], qo) and np.array_equal(b[[0, 2, 1, 3, 4]], ko)
+    # q and k use their own weights
+    a, b = oracle.qk_norm_rope(q, k, pos, kw, qw)
+    assert not np.array_equal(a, qo)

@@ -11,7 +11,9 @@ import pytest
 ROOT = Path(__file__).resolve().parent.parent
 PLANTS = ["ORC_PLANT_SLOT_OFFSET", "ORC_PLANT_GQA_MODULO", "ORC_PLANT_NO_SCALE",
           "ORC_PLANT_CAUSAL_OFF_BY_ONE", "ORC_PLANT_NO_RESCALE", "ORC_PLANT_KEEP_PADDING",
-          "ORC_PLANT_V_REVERSED"]
+          "ORC_PLANT_V_REVERSED", "ORC_PLANT_ROUND_TRUNC", "ORC_PLANT_NORM_SUM",
+          "ORC_PLANT_EPS_OUTSIDE", "ORC_PLANT_ROPE_INTERLEAVED", "ORC_PLANT_ROPE_FREQ",
+          "ORC_PLANT_ROPE_SIGN"]
 
 
 def test_unplanted_oracle_passes_the_pins():

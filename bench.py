@@ -219,6 +219,43 @@ class DecodeStep:
             ev[1].record()
 
 
+class PrologueStep:
+    """qk_norm_rope_store over a prefill step's tokens: QK-Norm and RoPE of
+    the projected q/k (views of one fused qkv buffer) with the store of the
+    rotated k and of v into the paged caches."""
+
+    def __init__(self, work, seed: int, theta: float = 1e6):
+        from paged_kv_cache_303_gb300 import ops, workloads as W
+        self.ops, self.work, h = ops, work, work.heads
+        n, hq, hkv, d = work.total_q, h.num_heads, h.num_kv_heads, h.head_dim
+        self.qkv = W.fill_normal_(torch.empty((n, hq + 2 * hkv, d), dtype=torch.bfloat16,
+                                              device="cuda"), seed)
+        self.q, self.k, self.v = self.qkv[:, :hq], self.qkv[:, hq:hq + hkv], self.qkv[:, hq + hkv:]
+        lens = (work.cu_seqlens_q[1:] - work.cu_seqlens_q[:-1]).tolist()
+        self.pos = torch.cat([torch.arange(p, p + L, dtype=torch.int64)
+                              for p, L in zip(work.prefix_lens.tolist(), lens)]).cuda()
+        g = W.generator(seed + 1)
+        self.qw = torch.empty(d).uniform_(0.5, 1.5, generator=g).to(torch.bfloat16).cuda()
+        self.kw = torch.empty(d).uniform_(0.5, 1.5, generator=g).to(torch.bfloat16).cuda()
+        shape = (h.num_blocks, h.block_size, hkv, d)
+        self.kc = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+        self.vc = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+        self.slots = ops.kv_build_slot_mapping(work.block_tables.cuda(), work.prefix_lens.cuda(),
+                                               work.cu_seqlens_q.cuda(), h.block_size)
+        self.q_out = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
+        self.theta = theta
+        # q, k, v read; rotated q, k and v written; positions and slots read
+        self.bytes = n * ((hq + 2 * hkv) * d * 2 * 2 + 8 + 4)
+
+    def __call__(self, ev=None):
+        if ev is not None:
+            ev[0].record()
+        self.ops.qk_norm_rope_store(self.q, self.k, self.v, self.pos, self.qw, self.kw, self.kc,
+                                    self.vc, self.slots, 1e-6, self.theta, q_out=self.q_out)
+        if ev is not None:
+            ev[1].record()
+
+
 class PrefillStep:
     """kv_build_slot_mapping -> kv_store -> paged_attn_prefill on resident inputs."""
 
@@ -395,8 +432,8 @@ def run_ours(args, rank, world):
     hbm, tfl = float(pk["hbm_gbs"]), float(pk["bf16_tflops"])
     dev_index = int(os.environ.get("LOCAL_RANK", "0"))
 
-    # headline: Qwen3-shaped decode step
-    dec = DecodeStep(W.qwen3_decode(), cache_seed=401)
+    # headline: Qwen3-shaped decode step, store fused into the decode launch
+    dec = DecodeStep(W.qwen3_decode(), cache_seed=401, fused=True)
     for _ in range(3):
         dec()
     torch.cuda.synchronize()
@@ -417,7 +454,7 @@ def run_ours(args, rank, world):
     ms_per_step = total_ms / args.steps
     value = dec.bytes * world * args.steps / (total_ms / 1e3) / 1e9
     eager_value = dec.bytes * world * args.steps / (eager_ms / 1e3) / 1e9
-    dec_achieved = (dec.bytes + dec.qo_bytes) / (dec_ms / 1e3) / 1e9
+    dec_achieved = (dec.bytes + dec.qo_bytes + dec.store_bytes) / (dec_ms / 1e3) / 1e9
 
     # end to end, host buffers
     e2e_ms, h2d, d2h = e2e_decode(dec, graph, args.steps, args.warmup, world)
@@ -428,27 +465,27 @@ def run_ours(args, rank, world):
     torch.cuda.empty_cache()
 
     also = {}
-    # the same step with the store fused into the decode launch
-    fz = DecodeStep(W.qwen3_decode(), cache_seed=401, fused=True)
+    # the same step as separate launches: decode slots, kv_store, decode, merge
+    uf = DecodeStep(W.qwen3_decode(), cache_seed=401, fused=False)
     for _ in range(3):
-        fz()
-    fgraph = fz.capture()
-    f_tot, _, _ = time_steps(lambda ev=None: fgraph.replay(), args.steps, args.warmup, world,
+        uf()
+    ugraph = uf.capture()
+    u_tot, _, _ = time_steps(lambda ev=None: ugraph.replay(), args.steps, args.warmup, world,
                              kernel_events=False)
-    f_eager, f_ms, _ = time_steps(fz, args.steps, args.warmup, world)
-    f_bytes = fz.bytes + fz.qo_bytes + fz.store_bytes
-    also["decode_fused"] = {
-        "workload": "qwen3-decode-b64, step = paged_attn_decode_store (store + decode in one "
-                    "launch) + merge, replayed as one CUDA graph",
-        "gbs": round(fz.bytes * world * args.steps / (f_tot / 1e3) / 1e9, 1),
-        "eager_gbs": round(fz.bytes * world * args.steps / (f_eager / 1e3) / 1e9, 1),
-        "step_ms": round(f_tot / args.steps, 4), "kernel_ms": round(f_ms, 4),
+    u_eager, u_ms, _ = time_steps(uf, args.steps, args.warmup, world)
+    u_bytes = uf.bytes + uf.qo_bytes
+    also["decode_unfused"] = {
+        "workload": "qwen3-decode-b64, step = kv_build_decode_slots + kv_store + "
+                    "paged_attn_decode + merge (4 launches), replayed as one CUDA graph",
+        "gbs": round(uf.bytes * world * args.steps / (u_tot / 1e3) / 1e9, 1),
+        "eager_gbs": round(uf.bytes * world * args.steps / (u_eager / 1e3) / 1e9, 1),
+        "step_ms": round(u_tot / args.steps, 4), "kernel_ms": round(u_ms, 4),
         "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
-                     "achieved": round(f_bytes / (f_ms / 1e3) / 1e9, 1),
-                     "frac": round(f_bytes / (f_ms / 1e3) / 1e9 / hbm, 4)},
-        "launches_per_step": fz.launches,
+                     "achieved": round(u_bytes / (u_ms / 1e3) / 1e9, 1),
+                     "frac": round(u_bytes / (u_ms / 1e3) / 1e9 / hbm, 4)},
+        "launches_per_step": uf.launches,
     }
-    del fz, fgraph
+    del uf, ugraph
     torch.cuda.empty_cache()
     # varlen prefill step (packed k/v), 8 prompts of U[128, 4096]
     pre = PrefillStep(W.varlen_prefill(), cache_seed=501)
@@ -469,6 +506,19 @@ def run_ours(args, rank, world):
         "bytes_per_launch": pre.store_bytes,
     }
     del pre
+    torch.cuda.empty_cache()
+    # QK-Norm + RoPE fused with the store, same tokens
+    pro = PrologueStep(W.varlen_prefill(), seed=511)
+    _, pro_ms, _ = time_steps(pro, args.steps, args.warmup, world)
+    also["qk_norm_rope_store"] = {
+        "workload": "QK-Norm + RoPE + K/V store of the varlen-prefill step's %d tokens "
+                    "(16q/8kv/128d, theta 1e6)" % pro.work.total_q,
+        "gbs": round(pro.bytes / (pro_ms / 1e3) / 1e9, 1), "kernel_ms": round(pro_ms, 4),
+        "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                     "frac": round(pro.bytes / (pro_ms / 1e3) / 1e9 / hbm, 4)},
+        "bytes_per_launch": pro.bytes,
+    }
+    del pro
     torch.cuda.empty_cache()
     # prefix-cache prefill
     pp = PrefillStep(W.prefix_prefill(), cache_seed=601)
@@ -518,8 +568,8 @@ def run_ours(args, rank, world):
         "data": "synthetic",
         "config": {"workload": "qwen3-decode-b64: 16q/8kv heads, head_dim 128, block_size 256, "
                                "batch 64, ctx U[512,4096], 2048-block pool, seed 304",
-                   "step": "decode slots + kv_store + paged_attn_decode (split + merge), "
-                           "replayed as one CUDA graph",
+                   "step": "paged_attn_decode_store (decode slot + K/V store + split "
+                           "decode in one launch) + merge, replayed as one CUDA graph",
                    "eager_value_gbs": round(eager_value, 1),
                    "l2": "no flush: the %.2f GB KV read per step exceeds the 129 MB L2" % (dec_bytes / 1e9),
                    "parallelism": f"replicas x{world}"},
@@ -528,7 +578,7 @@ def run_ours(args, rank, world):
         "gpu_launches": dec_launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(dec_achieved, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(dec_achieved / hbm, 4), "traffic": traffic,
-                     "kernel": "paged_attn_decode (split kernel + merge kernel)",
+                     "kernel": "paged_attn_decode_store (split kernel + merge kernel)",
                      "kernel_ms": round(dec_ms, 4), "peak_source": f"{pk_kind} hbm_gbs"},
         "cpu_baseline": cpu,
         "clocks": clk,

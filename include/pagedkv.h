@@ -149,6 +149,43 @@ int kv_store(const pkv_bf16 *key, int64_t key_row_stride,
              pkv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * qk_norm_rope_store -- L17 §4 (QK-Norm, then RoPE, on q and k; v as is)
+ * fused with the store of §5.1 / Lesson 04 §3.
+ *
+ * For every token n and head h (q: num_heads heads, k: num_kv_heads):
+ *   RMSNorm (layernorm module of "Nano-VLLM full-code notes (5)"):
+ *     y = bf16( bf16( x / sqrt(mean(x^2) + rms_eps) ) * w )   (fp32 inside)
+ *     with w = q_norm_weight or k_norm_weight [head_dim] bf16;
+ *   RoPE (RoFormer, rotate-half pairing; the pages apply it, L17 §4, but do
+ *   not print it): element e < head_dim/2 pairs with e + head_dim/2, pair i
+ *   turns by a_i = positions[n] * rope_theta^(-2i/head_dim):
+ *     out[i]       = y[i] cos a_i - y[i + d/2] sin a_i
+ *     out[i + d/2] = y[i + d/2] cos a_i + y[i] sin a_i      (fp32, then bf16)
+ * Rotated q goes to q_out; rotated k goes to k_out when k_out != NULL, and,
+ * with v unchanged, to the caches at slot_mapping[n] exactly as kv_store
+ * does (-1 skips the cache write; any other slot outside [0, num_slots) is
+ * skipped and sets PKV_STATUS_BAD_SLOT).
+ *   q [num_tokens, num_heads, head_dim], k and v [num_tokens, num_kv_heads,
+ *   head_dim], all bf16 with free row strides (multiples of 8 elements,
+ *   16-byte aligned), for example views into one fused qkv projection.
+ *   positions [num_tokens] int64 (absolute positions).
+ *   q_out may be q itself (same row stride), k_out may be k; otherwise the
+ *   outputs must not overlap the inputs.
+ * Supported: head_dim 64 or 128.  Positions are exact up to 2^24.
+ * ---------------------------------------------------------------------- */
+int qk_norm_rope_store(const pkv_bf16 *q, int64_t q_row_stride,
+                       const pkv_bf16 *k, int64_t k_row_stride,
+                       const pkv_bf16 *v, int64_t v_row_stride,
+                       const int64_t *positions,
+                       const pkv_bf16 *q_norm_weight, const pkv_bf16 *k_norm_weight,
+                       float rms_eps, float rope_theta,
+                       pkv_bf16 *q_out, int64_t q_out_row_stride,
+                       pkv_bf16 *k_out, int64_t k_out_row_stride,
+                       pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *slot_mapping,
+                       int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int64_t num_slots, pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * paged_attn_prefill -- L17 §5.2/§5.3 (flash_attn_varlen_func with
  * causal=True), Lesson 04 §4.
  *

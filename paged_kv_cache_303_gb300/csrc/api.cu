@@ -5,6 +5,7 @@
 // query.  No entry point allocates device memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -205,6 +206,70 @@ int kv_store(const pkv_bf16 *key, int64_t key_row_stride, const pkv_bf16 *value,
                                          v_cache, slot_mapping, num_tokens, D, num_slots, s);
     if (e != cudaSuccess) return cuda_fail(e, "kv_store");
     return post_launch(s, "kv_store");
+}
+
+int qk_norm_rope_store(const pkv_bf16 *q, int64_t q_row_stride, const pkv_bf16 *k,
+                       int64_t k_row_stride, const pkv_bf16 *v, int64_t v_row_stride,
+                       const int64_t *positions, const pkv_bf16 *q_norm_weight,
+                       const pkv_bf16 *k_norm_weight, float rms_eps, float rope_theta,
+                       pkv_bf16 *q_out, int64_t q_out_row_stride, pkv_bf16 *k_out,
+                       int64_t k_out_row_stride, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                       const int32_t *slot_mapping, int32_t num_tokens, int32_t num_heads,
+                       int32_t num_kv_heads, int32_t head_dim, int64_t num_slots,
+                       pkv_stream_t stream) {
+    const char *what = "qk_norm_rope_store";
+    if (num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_slots < 0)
+        return fail(PKV_ERR_INVALID_ARG, "%s: negative or zero sizes", what);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(PKV_ERR_UNSUPPORTED, "%s: head_dim must be 64 or 128", what);
+    if (!(rms_eps >= 0.f) || !(rope_theta > 0.f) || !(rope_theta < HUGE_VALF))
+        return fail(PKV_ERR_INVALID_ARG, "%s: need rms_eps >= 0 and a finite rope_theta > 0", what);
+    if (num_tokens == 0) return ok();
+    if (!q || !k || !v || !positions || !q_norm_weight || !k_norm_weight || !q_out || !k_cache ||
+        !v_cache || !slot_mapping)
+        return fail(PKV_ERR_INVALID_ARG, "%s: null pointer", what);
+    const int64_t qrow = (int64_t)num_heads * head_dim, kvrow = (int64_t)num_kv_heads * head_dim;
+    if (q_row_stride < qrow || q_out_row_stride < qrow || k_row_stride < kvrow ||
+        v_row_stride < kvrow || (k_out && k_out_row_stride < kvrow))
+        return fail(PKV_ERR_INVALID_ARG, "%s: a row stride is below heads*head_dim", what);
+    if (q_row_stride % 8 || q_out_row_stride % 8 || k_row_stride % 8 || v_row_stride % 8 ||
+        (k_out && k_out_row_stride % 8) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(q_out) || (k_out && !aligned16(k_out)) || !aligned16(k_cache) ||
+        !aligned16(v_cache) || !aligned16(q_norm_weight) || !aligned16(k_norm_weight))
+        return fail(PKV_ERR_UNSUPPORTED,
+                    "%s: tensors must be 16-byte aligned with row strides a multiple of 8", what);
+    if ((q_out == q && q_out_row_stride != q_row_stride) ||
+        (k_out && k_out == k && k_out_row_stride != k_row_stride))
+        return fail(PKV_ERR_INVALID_ARG, "%s: an in-place output must keep its input's row stride",
+                    what);
+    pkv::PrologueArgs a{};
+    a.q = q;
+    a.q_rs = q_row_stride;
+    a.k = k;
+    a.k_rs = k_row_stride;
+    a.v = v;
+    a.v_rs = v_row_stride;
+    a.positions = positions;
+    a.q_weight = q_norm_weight;
+    a.k_weight = k_norm_weight;
+    a.eps = rms_eps;
+    a.theta = rope_theta;
+    a.q_out = q_out;
+    a.q_out_rs = q_out_row_stride;
+    a.k_out = k_out;
+    a.k_out_rs = k_out_row_stride;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.slots = slot_mapping;
+    a.num_slots = num_slots;
+    a.num_tokens = num_tokens;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = pkv::launch_qk_norm_rope_store(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return post_launch(s, what);
 }
 
 size_t paged_attn_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t num_kv_heads,

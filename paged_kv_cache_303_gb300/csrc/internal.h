@@ -29,6 +29,27 @@ cudaError_t launch_kv_store(const uint16_t *key, int64_t key_rs, const uint16_t 
                             int64_t value_rs, uint16_t *kc, uint16_t *vc, const int32_t *slots,
                             int32_t n, int64_t D, int64_t num_slots, cudaStream_t stream);
 
+struct PrologueArgs {
+    const uint16_t *q;
+    int64_t q_rs;
+    const uint16_t *k;
+    int64_t k_rs;
+    const uint16_t *v;
+    int64_t v_rs;
+    const int64_t *positions;
+    const uint16_t *q_weight, *k_weight;
+    float eps, theta;
+    uint16_t *q_out;
+    int64_t q_out_rs;
+    uint16_t *k_out;
+    int64_t k_out_rs;
+    uint16_t *k_cache, *v_cache;
+    const int32_t *slots;
+    int64_t num_slots;
+    int32_t num_tokens, num_heads, num_kv_heads, head_dim;
+};
+cudaError_t launch_qk_norm_rope_store(const PrologueArgs &a, cudaStream_t stream);
+
 // ---- decode.cu ------------------------------------------------------------
 struct DecodeArgs {
     const uint16_t *q;

@@ -45,6 +45,8 @@ SIGNATURES = {
     "kv_build_slot_mapping": ([_P, _I64, _I32, _P, _P, _I32, _I32, _P, _I32, _P], _INT),
     "kv_build_decode_slots": ([_P, _I64, _I32, _P, _I32, _I32, _P, _P], _INT),
     "kv_store": ([_P, _I64, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _I64, _P], _INT),
+    "qk_norm_rope_store": ([_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _F32, _F32, _P, _I64, _P,
+                            _I64, _P, _P, _P, _I32, _I32, _I32, _I32, _I64, _P], _INT),
     "paged_attn_prefill": ([_P, _I64, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _I32, _P, _P,
                             _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _I64,
                             _P, _P, _SZ, _P], _INT),
@@ -189,6 +191,46 @@ def kv_store(key, value, k_cache, v_cache, slot_mapping):
         raise ValueError("cache sizes do not match num_kv_heads * head_dim")
     _check(lib().kv_store(_ptr(key), krs, _ptr(value), vrs, _ptr(k_cache), _ptr(v_cache),
                           _ptr(slots), n, hkv, d, num_slots, _stream(key.device)))
+
+
+def qk_norm_rope_store(q, k, v, positions, q_norm_weight, k_norm_weight, k_cache, v_cache,
+                       slot_mapping, eps: float = 1e-6, theta: float = 1e6,
+                       q_out: Optional[torch.Tensor] = None, k_out: Optional[torch.Tensor] = None):
+    """QK-Norm then RoPE on q [N, Hq, d] and k [N, Hkv, d], fused with the
+    store of the rotated k and of v [N, Hkv, d] into the paged caches.
+    Returns (q_out, k_out); q_out=q (and k_out=k) rotate in place; k_out None
+    writes rotated k only to the cache."""
+    qrs, krs, vrs = _rows(q, "q"), _rows(k, "k"), _rows(v, "v")
+    n, hq, d = q.shape
+    hkv = k.shape[1]
+    if tuple(k.shape) != (n, hkv, d) or tuple(v.shape) != (n, hkv, d):
+        raise ValueError("q, k, v must be [N, heads, head_dim] with the same N and head_dim")
+    _cuda(k_cache, torch.bfloat16, "k_cache")
+    _cuda(v_cache, torch.bfloat16, "v_cache")
+    if k_cache.shape != v_cache.shape or k_cache.shape[2:] != (hkv, d) or not k_cache.is_contiguous() \
+            or not v_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, d]")
+    pos = positions
+    if pos.dtype != torch.int64 or pos.device != q.device or not pos.is_contiguous() or pos.numel() != n:
+        raise ValueError("positions must be a contiguous int64 CUDA tensor with one entry per token")
+    for w, name in ((q_norm_weight, "q_norm_weight"), (k_norm_weight, "k_norm_weight")):
+        _cuda(w, torch.bfloat16, name)
+        if w.numel() != d or not w.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [head_dim] bf16 tensor")
+    slots = _i32(slot_mapping, "slot_mapping")
+    if slots.numel() != n:
+        raise ValueError("slot_mapping must have one entry per token")
+    if q_out is None:
+        q_out = torch.empty((n, hq, d), dtype=torch.bfloat16, device=q.device)
+    qors = _rows(q_out, "q_out")
+    kors = _rows(k_out, "k_out") if k_out is not None else 0
+    num_slots = k_cache.shape[0] * k_cache.shape[1]
+    _check(lib().qk_norm_rope_store(_ptr(q), qrs, _ptr(k), krs, _ptr(v), vrs, _ptr(pos),
+                                    _ptr(q_norm_weight), _ptr(k_norm_weight), float(eps),
+                                    float(theta), _ptr(q_out), qors, _ptr(k_out), kors,
+                                    _ptr(k_cache), _ptr(v_cache), _ptr(slots), n, hq, hkv, d,
+                                    num_slots, _stream(q.device)))
+    return q_out, k_out
 
 
 def decode_workspace_size(batch, num_heads, num_kv_heads, head_dim, max_context_len) -> int:

@@ -168,7 +168,8 @@ int kv_store(const pkv_bf16 *key, int64_t key_row_stride,
  *   q [num_tokens, num_heads, head_dim], k and v [num_tokens, num_kv_heads,
  *   head_dim], all bf16 with free row strides (multiples of 8 elements,
  *   16-byte aligned), for example views into one fused qkv projection.
- *   positions [num_tokens] int64 (absolute positions).
+ *   positions [num_tokens] int64 (absolute positions; int64 as in Lesson 04
+ *   §1).
  *   q_out may be q itself (same row stride), k_out may be k; otherwise the
  *   outputs must not overlap the inputs.
  * Supported: head_dim 64 or 128.  Positions are exact up to 2^24.

@@ -1,10 +1,17 @@
 """Parity of qk_norm_rope_store (QK-Norm, RoPE and the K/V store in one
 launch; L17 §4 then §5.1) with the oracle.
 
-The rotated q and k must satisfy |gpu - oracle| <= 1e-2 + 1e-2 * |oracle|
-elementwise (bf16 outputs of fp32 arithmetic against fp64 with the same two
-bf16 roundings); the cache must hold exactly the k the kernel returned and
-exactly the input v at every stored slot, and nothing anywhere else.
+Tolerance, derived from the arithmetic: the RMSNorm of "Nano-VLLM full-code
+notes (5)" rounds to bf16 twice (the normalised value, then its product with
+the weight) from fp32 values.  The GPU and the oracle (fp64) agree on those
+roundings except where the exact value sits within a few fp32 ulps of a bf16
+rounding boundary; there one side may land one bf16 ulp away, and RoPE mixes
+that input of the pair into both outputs.  So element e of a pair with
+magnitude r = sqrt(out_e^2 + out_partner^2) must satisfy
+    |gpu - oracle| <= 1e-2 + 1e-2 * |oracle| + 2 * ulp_bf16(r),
+and at least 97% of all elements must be bit-identical.  The cache must
+hold exactly the k the kernel returned and exactly the input v at every
+stored slot, and nothing anywhere else.
 """
 import math
 
@@ -50,6 +57,30 @@ def _inputs(n, hq, hkv, d, seed, num_slots, pad_every=0, max_pos=32767):
     return qkv, pos, qw, kw, slots
 
 
+def _ulp_bf16(x):
+    """spacing of bf16 numbers at magnitude x (8 significant bits)"""
+    x = np.maximum(np.abs(x), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(x)) - 7)
+
+
+def assert_rotated_close(gpu: torch.Tensor, ref_bits: np.ndarray, what: str):
+    g = gpu.detach().float().cpu().double().numpy()
+    ref = f64(ref_bits)
+    assert g.shape == ref.shape
+    h = ref.shape[-1] // 2
+    partner = np.concatenate([ref[..., h:], ref[..., :h]], axis=-1)
+    bound = 1e-2 + 1e-2 * np.abs(ref) + 2 * _ulp_bf16(np.hypot(ref, partner))
+    err = np.abs(g - ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)[:5].tolist()
+        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside tolerance, "
+                             f"max abs {np.nanmax(err):.3e}, first bad {idx}")
+    same = float((bits(gpu) == ref_bits).mean())
+    print(f"{what}: bit-identical fraction {same:.6f}, max abs {err.max():.3e}")
+    assert same > 0.97, same
+
+
 def _oracle(qkv, pos, qw, kw, hq, hkv, eps, theta):
     q, k = bits(qkv[:, :hq]), bits(qkv[:, hq:hq + hkv])
     return oracle.qk_norm_rope(q, k, pos.numpy(), bits(qw), bits(kw), eps, theta)
@@ -92,11 +123,8 @@ def test_prologue_vs_oracle(hq, hkv, d, n, theta):
                                           k_out=torch.empty((n, hkv, d), dtype=torch.bfloat16,
                                                             device="cuda"))
     torch.cuda.synchronize()
-    assert_close(q_out, f64(ref_q), "rotated q")
-    assert_close(k_out, f64(ref_k), "rotated k")
-    # most elements agree to the bit; the rest differ by a rounding flip
-    same = (bits(q_out) == ref_q).mean()
-    assert same > 0.97, same
+    assert_rotated_close(q_out, ref_q, "rotated q")
+    assert_rotated_close(k_out, ref_k, "rotated k")
     _check_cache(gk, gv, slots, bits(k_out), bits(qkv[:, hq + hkv:]), num_slots)
 
 
@@ -144,10 +172,10 @@ def test_prologue_full_size_varlen_step():
     q_out, _ = ops.qk_norm_rope_store(gq[:, :hq], gq[:, hq:hq + hkv], gq[:, hq + hkv:], dev(pos),
                                       dev(qw), dev(kw), gk, gv, dev(torch.from_numpy(slots)))
     torch.cuda.synchronize()
-    assert_close(q_out, f64(ref_q), "rotated q, full size")
+    assert_rotated_close(q_out, ref_q, "rotated q, full size")
     cached_k = bits(gk).reshape(num_slots, hkv, h.head_dim)[slots]
-    assert_close(torch.from_numpy(cached_k.view(np.int16)).view(torch.bfloat16), f64(ref_k),
-                 "rotated k in the cache, full size")
+    assert_rotated_close(torch.from_numpy(cached_k.view(np.int16)).view(torch.bfloat16), ref_k,
+                         "rotated k in the cache, full size")
     _check_cache(gk, gv, torch.from_numpy(slots), cached_k, bits(qkv[:, hq + hkv:]), num_slots)
 
 

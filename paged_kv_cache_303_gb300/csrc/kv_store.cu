@@ -172,22 +172,33 @@ __global__ void __launch_bounds__(kStoreWarps * 32) kv_store_scalar_kernel(
 // pos * theta^(-2i/d); the rotation is computed in fp32 from the bf16 norm
 // output and rounded to bf16 once.
 //
-// A warp owns a token: a row of head_dim bf16 is HD/8 lanes x 16 bytes, so a
-// warp-wide vector load covers 32/(HD/8) rows and all of the token's
-// Hq + 2*Hkv rows take a few passes of kProUnroll loads per lane, issued
-// before any arithmetic.  Each lane holds the same 8 element positions of
-// every row, so it computes the 8 (cos, sin) pairs of those positions once
-// per token; the RMS sum is reduced over the row's lanes and the rotation
-// partner (element e +- d/2) is HD/16 lanes away (one xor shuffle).
-// The angle pos * f_i is formed as pos * f_hi + (error of that product +
-// pos * f_lo) with f_hi + f_lo = theta^(-2i/d) computed on the host in
-// double, so the angle carries no fp32 rounding of f_i or of the product;
-// sincosf of the rounded part is then corrected to first order by the rest.
+// Lane layout: a lane holds 8 elements e .. e+7 of the first half of a row
+// and their rotation partners e+d/2 .. (two 16-byte pieces), so a row is
+// d/16 lanes, the RMS sum is reduced over d/16 lanes by xor shuffles, and
+// the rotation needs no exchange between lanes.
+// Work unit: one warp takes kProUnroll warp-wide passes of one token's rows
+// (a pass covers 32/(d/16) rows): 12 rows at head_dim 128, so a Qwen3 token
+// (16 q + 8 k + 8 v rows) is three units.  One resident wave of CTAs; each
+// warp walks its units and issues all loads of the next unit before
+// computing the current one, so two units' loads are in flight per warp.
+// The unit's (cos, sin) of the d/2 pair angles are computed two per lane
+// and handed to the lanes that need them by shuffles.  The angle pos * f_i
+// is formed as pos * f_hi + (error of that product + pos * f_lo) with
+// f_hi + f_lo = theta^(-2i/d) computed on the host in double, so the angle
+// carries no fp32 rounding of f_i or of the product; sincosf of the rounded
+// part is then corrected to first order by the rest.  Value rows are copied
+// as they are.
 // HBM-bound: per token it reads (Hq + 2*Hkv) * d * 2 bytes and writes
 // (Hq + 2*Hkv) * d * 2 bytes (+ Hkv * d * 2 when k is also written back).
 // ---------------------------------------------------------------------------
+#ifndef PKV_PRO_UNROLL
+#define PKV_PRO_UNROLL 3      // warp-wide passes per work unit
+#endif
+#ifndef PKV_PRO_MIN_CTAS
+#define PKV_PRO_MIN_CTAS 2
+#endif
 constexpr int kProWarps = 8;
-constexpr int kProUnroll = 4;
+constexpr int kProUnroll = PKV_PRO_UNROLL;
 
 struct PrologueParams {
     const uint16_t *q;
@@ -207,125 +218,183 @@ struct PrologueParams {
     const int32_t *slots;
     int64_t num_slots;
     int32_t n, hq, hkv;
+    int32_t chunks;              // units per token
     float inv_hi[64], inv_lo[64];
 };
 
-__device__ __forceinline__ float round_bf16(float x) {
-    return bf16lo_to_f32(pack_bf16x2(x, 0.f));
+// bf16 x bf16 -> bf16 for a packed pair (the exact product, rounded once)
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
+    return make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w));
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kProWarps * 32)
+__global__ void __launch_bounds__(kProWarps * 32, PKV_PRO_MIN_CTAS)
 qk_norm_rope_store_kernel(const __grid_constant__ PrologueParams p) {
-    constexpr int LPR = HD / 8;                 // lanes per row
-    constexpr int RPW = 32 / LPR;               // rows per warp-wide pass
     constexpr int HALF = HD / 2;
+    constexpr int LPR = HD / 16;                // lanes per row
+    constexpr int RPW = 32 / LPR;               // rows per warp-wide pass
     const int lane = threadIdx.x & 31;
     const int sub = lane / LPR;
-    const int e0 = (lane % LPR) * 8;            // this lane's elements e0 .. e0+7
-    const bool first = e0 < HALF;
-    const int i0 = e0 % HALF;                   // and their pair indices
-
-    float wq[8], wk[8];
-    {
-        const uint4 a = *reinterpret_cast<const uint4 *>(p.qw + e0);
-        const uint4 b = *reinterpret_cast<const uint4 *>(p.kw + e0);
-        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            wq[2 * j] = bf16lo_to_f32(av[j]);
-            wq[2 * j + 1] = bf16hi_to_f32(av[j]);
-            wk[2 * j] = bf16lo_to_f32(bv[j]);
-            wk[2 * j + 1] = bf16hi_to_f32(bv[j]);
-        }
-    }
+    // this lane's elements: ea .. ea+7 and their rotation partners ea+d/2 ..,
+    // so pair i = ea + j is (element i, element i + d/2) in one lane
+    const int ea = (lane % LPR) * 8;
+    const int64_t total = (int64_t)p.n * p.chunks;
+    const int64_t stride = (int64_t)gridDim.x * kProWarps;
+    int64_t unit = (int64_t)blockIdx.x * kProWarps + (threadIdx.x >> 5);
+    if (unit >= total) return;                  // uniform per warp
     const int rows = p.hq + 2 * p.hkv;
     const int64_t D = (int64_t)p.hkv * HD;
+    // both norms' weights for this lane's elements, packed bf16
+    const uint4 wqa = ld_stream_v4(p.qw + ea), wqb = ld_stream_v4(p.qw + HALF + ea);
+    const uint4 wka = ld_stream_v4(p.kw + ea), wkb = ld_stream_v4(p.kw + HALF + ea);
 
-    for (int64_t t = (int64_t)blockIdx.x * kProWarps + (threadIdx.x >> 5); t < p.n;
-         t += (int64_t)gridDim.x * kProWarps) {
-        const float pos = (float)p.pos[t];      // exact for positions below 2^24
-        float cs[8], sn[8];
+    // start the loads of a unit: its kProUnroll passes of rows, slot and position
+    auto load = [&](int64_t u_id, uint4 (&xa)[kProUnroll], uint4 (&xb)[kProUnroll],
+                    int64_t &slot, float &pos) {
+        const int64_t t = u_id / p.chunks;
+        const int r0 = (int)(u_id % p.chunks) * (RPW * kProUnroll);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float fh = p.inv_hi[i0 + j], fl = p.inv_lo[i0 + j];
-            const float ah = pos * fh;
-            const float al = fmaf(pos, fl, fmaf(pos, fh, -ah));
-            float s0, c0;
-            sincosf(ah, &s0, &c0);
-            sn[j] = fmaf(al, c0, s0);
-            cs[j] = fmaf(-al, s0, c0);
+        for (int u = 0; u < kProUnroll; ++u) {
+            const int r = r0 + u * RPW + sub;
+            const uint16_t *src = nullptr;
+            if (r < p.hq)
+                src = p.q + t * p.q_rs + (int64_t)r * HD;
+            else if (r < p.hq + p.hkv)
+                src = p.k + t * p.k_rs + (int64_t)(r - p.hq) * HD;
+            else if (r < rows)
+                src = p.v + t * p.v_rs + (int64_t)(r - p.hq - p.hkv) * HD;
+            xa[u] = src ? ld_stream_v4(src + ea) : make_uint4(0u, 0u, 0u, 0u);
+            xb[u] = src ? ld_stream_v4(src + HALF + ea) : make_uint4(0u, 0u, 0u, 0u);
         }
-        const int64_t slot = p.slots[t];
-        const bool store = slot >= 0 && slot < p.num_slots;
-        if (lane == 0 && !store && slot != -1) flag(PKV_STATUS_BAD_SLOT);
+        slot = p.slots[t];
+        pos = r0 < p.hq + p.hkv ? (float)p.pos[t] : 0.f;   // exact for positions below 2^24
+    };
 
-        for (int r0 = 0; r0 < rows; r0 += RPW * kProUnroll) {
-            uint4 x[kProUnroll];
+    uint4 xa[kProUnroll], xb[kProUnroll];
+    int64_t slot;
+    float pos;
+    load(unit, xa, xb, slot, pos);
+    for (;;) {
+        // the next unit's loads are in flight while this one is computed
+        const int64_t next = unit + stride;
+        uint4 na[kProUnroll], nb[kProUnroll];
+        int64_t slot_n = -1;
+        float pos_n = 0.f;
+        if (next < total) load(next, na, nb, slot_n, pos_n);
+
+        const int64_t t = unit / p.chunks;
+        const int r0 = (int)(unit % p.chunks) * (RPW * kProUnroll);
+        const bool store = slot >= 0 && slot < p.num_slots;
+        if (lane == 0 && r0 == 0 && !store && slot != -1) flag(PKV_STATUS_BAD_SLOT);
+
+        float cs[8], sn[8];
+        if (r0 < p.hq + p.hkv) {                // the unit rotates rows (warp-uniform)
+            // pairs 2*lane and 2*lane+1 (mod d/2) of the angle table
+            float c2[2], s2[2];
 #pragma unroll
-            for (int u = 0; u < kProUnroll; ++u) {
-                const int r = r0 + u * RPW + sub;
-                const uint16_t *src = nullptr;
-                if (r < p.hq)
-                    src = p.q + t * p.q_rs + (int64_t)r * HD;
-                else if (r < p.hq + p.hkv)
-                    src = p.k + t * p.k_rs + (int64_t)(r - p.hq) * HD;
-                else if (r < rows)
-                    src = p.v + t * p.v_rs + (int64_t)(r - p.hq - p.hkv) * HD;
-                x[u] = src ? ld_stream_v4(src + e0) : make_uint4(0u, 0u, 0u, 0u);
+            for (int h = 0; h < 2; ++h) {
+                const int i = (2 * lane + h) % HALF;
+                const float fh = p.inv_hi[i], fl = p.inv_lo[i];
+                const float ah = pos * fh;
+                const float al = fmaf(pos, fl, fmaf(pos, fh, -ah));
+                float s0, c0;
+                sincosf(ah, &s0, &c0);
+                s2[h] = fmaf(al, c0, s0);
+                c2[h] = fmaf(-al, s0, c0);
             }
 #pragma unroll
-            for (int u = 0; u < kProUnroll; ++u) {
-                const int r = r0 + u * RPW + sub;
-                const bool is_q = r < p.hq;
-                const bool is_k = !is_q && r < p.hq + p.hkv;
-                const uint32_t xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-                float xf[8];
+            for (int jj = 0; jj < 4; ++jj) {
+                const int src = ea / 2 + jj;    // lane holding pairs ea + 2jj, ea + 2jj + 1
+                cs[2 * jj] = __shfl_sync(0xffffffffu, c2[0], src);
+                cs[2 * jj + 1] = __shfl_sync(0xffffffffu, c2[1], src);
+                sn[2 * jj] = __shfl_sync(0xffffffffu, s2[0], src);
+                sn[2 * jj + 1] = __shfl_sync(0xffffffffu, s2[1], src);
+            }
+        }
+
+#pragma unroll
+        for (int u = 0; u < kProUnroll; ++u) {
+            const int r = r0 + u * RPW + sub;
+            const bool is_q = r < p.hq;
+            const bool is_k = !is_q && r < p.hq + p.hkv;
+            if (r0 + u * RPW < p.hq + p.hkv) {  // some row of this pass rotates (warp-uniform)
+                const uint32_t av[4] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w};
+                const uint32_t bv[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+                float2 fa[4], fb[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    xf[2 * j] = bf16lo_to_f32(xv[j]);
-                    xf[2 * j + 1] = bf16hi_to_f32(xv[j]);
+                    fa[j] = unpack_bf16x2(av[j]);
+                    fb[j] = unpack_bf16x2(bv[j]);
                 }
                 // every lane takes part in the shuffles, whatever its row is
-                float ss = 0.f;
+                float2 ss2 = fmul2(fa[0], fa[0]);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) ss = fmaf(xf[j], xf[j], ss);
+                for (int j = 1; j < 4; ++j) ss2 = ffma2(fa[j], fa[j], ss2);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ss2 = ffma2(fb[j], fb[j], ss2);
+                float ss = ss2.x + ss2.y;
 #pragma unroll
                 for (int off = LPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
                 const float inv = rsqrtf(ss * (1.f / HD) + p.eps);
-                uint32_t yp[4];
+                const float2 inv2 = make_float2(inv, inv);
+                const uint4 wa = is_q ? wqa : wka, wb = is_q ? wqb : wkb;
+                const uint32_t wav[4] = {wa.x, wa.y, wa.z, wa.w}, wbv[4] = {wb.x, wb.y, wb.z, wb.w};
+                uint32_t oa[4], ob[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float w0 = is_q ? wq[2 * j] : wk[2 * j];
-                    const float w1 = is_q ? wq[2 * j + 1] : wk[2 * j + 1];
-                    yp[j] = pack_bf16x2(round_bf16(xf[2 * j] * inv) * w0,
-                                        round_bf16(xf[2 * j + 1] * inv) * w1);
-                }
-                uint32_t pp[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) pp[j] = __shfl_xor_sync(0xffffffffu, yp[j], LPR / 2);
-                uint32_t ov[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float y0 = bf16lo_to_f32(yp[j]), y1 = bf16hi_to_f32(yp[j]);
-                    const float q0 = bf16lo_to_f32(pp[j]), q1 = bf16hi_to_f32(pp[j]);
+                    // y = bf16(bf16(x * inv) * w), the two roundings of the norm
+                    const float2 na2 = fmul2(fa[j], inv2), nb2 = fmul2(fb[j], inv2);
+                    const float2 ya = unpack_bf16x2(mul_bf16x2(pack_bf16x2(na2.x, na2.y), wav[j]));
+                    const float2 yb = unpack_bf16x2(mul_bf16x2(pack_bf16x2(nb2.x, nb2.y), wbv[j]));
+                    const float2 c = make_float2(cs[2 * j], cs[2 * j + 1]);
+                    const float2 sv = make_float2(sn[2 * j], sn[2 * j + 1]);
                     // first half: y cos - partner sin; second half: y cos + partner sin
-                    const float s0 = first ? -sn[2 * j] : sn[2 * j];
-                    const float s1 = first ? -sn[2 * j + 1] : sn[2 * j + 1];
-                    ov[j] = pack_bf16x2(fmaf(q0, s0, y0 * cs[2 * j]), fmaf(q1, s1, y1 * cs[2 * j + 1]));
+                    const float2 ra = ffma2(yb, make_float2(-sv.x, -sv.y), fmul2(ya, c));
+                    const float2 rb = ffma2(ya, sv, fmul2(yb, c));
+                    oa[j] = pack_bf16x2(ra.x, ra.y);
+                    ob[j] = pack_bf16x2(rb.x, rb.y);
                 }
-                const uint4 o = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+                const uint4 oA = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+                const uint4 oB = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+                uint16_t *dst = nullptr, *dst2 = nullptr;
                 if (is_q) {
-                    st_v4(p.q_out + t * p.q_out_rs + (int64_t)r * HD + e0, o);
+                    dst = p.q_out + t * p.q_out_rs + (int64_t)r * HD;
                 } else if (is_k) {
                     const int h = r - p.hq;
-                    if (p.k_out) st_v4(p.k_out + t * p.k_out_rs + (int64_t)h * HD + e0, o);
-                    if (store) st_v4(p.kc + slot * D + (int64_t)h * HD + e0, o);
-                } else if (r < rows && store) {
-                    st_v4(p.vc + slot * D + (int64_t)(r - p.hq - p.hkv) * HD + e0, x[u]);
+                    if (p.k_out) dst = p.k_out + t * p.k_out_rs + (int64_t)h * HD;
+                    if (store) dst2 = p.kc + slot * D + (int64_t)h * HD;
+                }
+                if (dst) {
+                    st_v4(dst + ea, oA);
+                    st_v4(dst + HALF + ea, oB);
+                }
+                if (dst2) {
+                    st_v4(dst2 + ea, oA);
+                    st_v4(dst2 + HALF + ea, oB);
                 }
             }
+            if (!is_q && !is_k && r < rows && store) {
+                uint16_t *dst = p.vc + slot * D + (int64_t)(r - p.hq - p.hkv) * HD;
+                st_v4(dst + ea, xa[u]);
+                st_v4(dst + HALF + ea, xb[u]);
+            }
         }
+
+        if (next >= total) break;
+        unit = next;
+#pragma unroll
+        for (int u = 0; u < kProUnroll; ++u) {
+            xa[u] = na[u];
+            xb[u] = nb[u];
+        }
+        slot = slot_n;
+        pos = pos_n;
     }
 }
 
@@ -359,7 +428,14 @@ cudaError_t launch_qk_norm_rope_store(const PrologueArgs &a, cudaStream_t stream
         p.inv_hi[i] = (float)f;
         p.inv_lo[i] = (float)(f - (double)p.inv_hi[i]);
     }
-    const dim3 grid((a.num_tokens + kProWarps - 1) / kProWarps);
+    const int rows_per_unit = (32 / (a.head_dim / 16)) * kProUnroll;
+    p.chunks = (a.num_heads + 2 * a.num_kv_heads + rows_per_unit - 1) / rows_per_unit;
+    // one resident wave of CTAs; each warp walks its units with the next
+    // unit's loads in flight
+    const int64_t units = (int64_t)a.num_tokens * p.chunks;
+    const int64_t need = (units + kProWarps - 1) / kProWarps;
+    const int64_t wave = (int64_t)num_sms() * PKV_PRO_MIN_CTAS;
+    const dim3 grid((unsigned)(need < wave ? need : wave));
     if (a.head_dim == 128)
         qk_norm_rope_store_kernel<128><<<grid, kProWarps * 32, 0, stream>>>(p);
     else

@@ -574,14 +574,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     for (int c = 0; c < kBN; ++c)
                         if (c > limit) sr[c] = __float_as_uint(-INFINITY);
                 }
-                // eight independent partial maxima keep the dependency chains short
+                // eight independent partial maxima keep the dependency chains
+                // short; three-input max takes two new scores per instruction
                 float pm[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) pm[i] = __uint_as_float(sr[i]);
 #pragma unroll
-                for (int c = 8; c < kBN; ++c) pm[c & 7] = fmaxf(pm[c & 7], __uint_as_float(sr[c]));
-                const float rmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                         fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+                for (int c = 8; c < kBN; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        pm[i] = fmax3(pm[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
+                const float rmax = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                                         fmaxf(pm[6], pm[7]));
                 const float m_new = fmaxf(m, rmax * sc);
                 const bool rescale = (m == -INFINITY) ? (m_new != -INFINITY)
                                                       : (m_new > m + kRescaleThreshold);

@@ -113,3 +113,32 @@ def test_product_never_imports_the_oracle():
             assert "import paged_kv_cache_303_gb300" not in text, f
             assert "from paged_kv_cache_303_gb300" not in text, f
             assert "libpagedkv" not in text and "pagedkv.h" not in text, f
+
+
+def test_fused_entry_points_validate_before_launch(lib):
+    p = ctypes.c_void_p(256)
+    # paged_attn_decode_store: key/value are required
+    rc = lib.paged_attn_decode_store(p, 256, None, 0, None, 0, p, p, 4, p, 1, 1, p, 1, 2, 1, 128,
+                                     16, 16, 0.1, p, 256, None, None, 0, None)
+    assert rc == 1 and "key" in _err(lib)
+    # ... with row strides that are not multiples of 8 elements
+    rc = lib.paged_attn_decode_store(p, 256, p, 132, p, 128, p, p, 4, p, 1, 1, p, 1, 2, 1, 128,
+                                     16, 16, 0.1, p, 256, None, None, 0, None)
+    assert rc == 2
+    # qk_norm_rope_store: head_dim 96 unsupported, theta must be positive
+    rc = lib.qk_norm_rope_store(p, 384, p, 96, p, 96, p, p, p, 1e-6, 1e6, p, 384, None, 0, p, p, p,
+                                4, 4, 1, 96, 64, None)
+    assert rc == 2 and "head_dim" in _err(lib)
+    rc = lib.qk_norm_rope_store(p, 512, p, 128, p, 128, p, p, p, 1e-6, 0.0, p, 512, None, 0, p, p, p,
+                                4, 4, 1, 128, 64, None)
+    assert rc == 1 and "theta" in _err(lib)
+    rc = lib.qk_norm_rope_store(p, 512, p, 128, p, 128, None, p, p, 1e-6, 1e6, p, 512, None, 0, p, p,
+                                p, 4, 4, 1, 128, 64, None)
+    assert rc == 1 and "null" in _err(lib)
+    # an in-place q_out must keep q's row stride
+    rc = lib.qk_norm_rope_store(p, 1024, p, 128, p, 128, p, p, p, 1e-6, 1e6, p, 512, None, 0, p, p,
+                                p, 4, 4, 1, 128, 64, None)
+    assert rc == 1 and "in-place" in _err(lib)
+    # zero tokens is a valid no-op
+    assert lib.qk_norm_rope_store(None, 0, None, 0, None, 0, None, None, None, 1e-6, 1e6, None, 0,
+                                  None, 0, None, None, None, 0, 4, 1, 128, 0, None) == 0

@@ -186,3 +186,46 @@ def test_decode_store_step_replayed_as_cuda_graph():
     ref, _ = oracle.decode(bits(nq), kref, vref, work.block_tables, work.context_lens, h.scale)
     assert_close(out, ref, "graph-replayed fused decode")
     assert np.array_equal(bits(gk), kref) and np.array_equal(bits(gv), vref)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_chunk_merge_with_dirty_workspace_twice(fused, monkeypatch):
+    """Chunks of 32 keys (up to 64 per sequence), a workspace full of 0xFF
+    bytes and two calls in a row on it: the chunk counters and partials must
+    not depend on what the workspace held before."""
+    monkeypatch.setenv("PKV_DECODE_CHUNK_TILES", "1")
+    heads = W.Heads(16, 8, 128, 64, 128)
+    ctx = [1, 31, 32, 33, 64, 65, 1000, 2047, 2048, 0, 7]
+    work = W.decode_work(heads, ctx, seed=880)
+    kc, vc = W.history_cache(heads, 881)
+    kref, vref = bits(kc).copy(), bits(vc).copy()
+    slots = oracle.decode_slots(work.block_tables, work.context_lens, heads.block_size)
+    oracle.kv_store(bits(work.k), bits(work.v), kref, vref, slots)
+    ref, ref_lse = oracle.decode(bits(work.q), kref, vref, work.block_tables, work.context_lens,
+                                 heads.scale)
+    gk, gv = dev(kc), dev(vc)
+    bt, gctx = dev(work.block_tables), dev(work.context_lens)
+    max_ctx = work.max_context_len
+    need = ops.decode_workspace_size(work.batch, heads.num_heads, heads.num_kv_heads,
+                                     heads.head_dim, max_ctx)
+    assert need > 0
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        if fused:
+            out, lse = ops.paged_attn_decode_store(dev(work.q), dev(work.k), dev(work.v), gk, gv, bt,
+                                                   gctx, max_ctx, heads.scale, workspace=ws,
+                                                   return_lse=True)
+        else:
+            ops.kv_store(dev(work.k), dev(work.v), gk, gv,
+                         ops.kv_build_decode_slots(bt, gctx, heads.block_size))
+            out, lse = ops.paged_attn_decode(dev(work.q), gk, gv, bt, gctx, max_ctx, heads.scale,
+                                             workspace=ws, return_lse=True)
+        torch.cuda.synchronize()
+        assert_close(out, ref, "decode with 1-tile chunks")
+        fin = np.isfinite(ref_lse)
+        got = lse.cpu().double().numpy()
+        assert np.array_equal(np.isfinite(got), fin)
+        assert np.allclose(got[fin], ref_lse[fin], atol=2e-3, rtol=1e-4)
+        outs.append(out.clone())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))

@@ -13,10 +13,12 @@
 //     (box: 64 head_dim elements x 1 head x min(block_size, 32) slots).  With
 //     block_size >= 8 the boxes use the 128-byte swizzle so that the
 //     row-per-lane reads below are bank-conflict free.
-//   * One producer warp keeps a 4-stage ring full (an mbarrier pair per
+//   * One producer warp keeps a 3-stage ring full (an mbarrier pair per
 //     stage); three consumer warps each take whole tiles in turn, with no
-//     CTA-wide barrier inside the loop.  Three CTAs share an SM, so that one
-//     CTA's start-up and merge overlap the others' streaming.
+//     CTA-wide barrier inside the loop.  Four CTAs share an SM (128
+//     registers a thread), so that one CTA's start-up and merge overlap the
+//     others' streaming: more CTAs per SM beat a deeper ring here (3 stages
+//     x 4 CTAs 5.21 TB/s, 4 x 3 5.08, 6 x 2 4.26 on the batch-64 workload).
 //   * Scores: lane = token; the lane dots its key row with the G queries
 //     (packed fp32x2 FMAs).  Scores carry scale*log2(e) so the softmax uses
 //     exp2.
@@ -74,10 +76,10 @@ namespace {
 #define PKV_DEC_CONSUMERS 3
 #endif
 #ifndef PKV_DEC_STAGES
-#define PKV_DEC_STAGES 4
+#define PKV_DEC_STAGES 3
 #endif
 #ifndef PKV_DEC_MIN_CTAS
-#define PKV_DEC_MIN_CTAS 3
+#define PKV_DEC_MIN_CTAS 4
 #endif
 constexpr int kConsumers = PKV_DEC_CONSUMERS;    // consumer warps per CTA
 constexpr int kThreads = (kConsumers + 1) * 32;  // + one TMA producer warp
@@ -585,12 +587,12 @@ void decode_plan(int32_t batch, int32_t num_kv_heads, int32_t head_dim, int32_t 
                  int32_t *chunk, int32_t *max_splits) {
     (void)head_dim;
     // about three waves of resident CTAs, assuming contexts average half of
-    // the maximum; chunks of 256 .. 4096 keys
+    // the maximum; chunks of 256 .. 2048 keys
     const int64_t keys = (int64_t)batch * num_kv_heads * max_context_len / 2;
     const int64_t target = (int64_t)num_sms() * PKV_DEC_MIN_CTAS * 3;
     int64_t per = (keys + target * kTile - 1) / (target * kTile);
     if (per < 8) per = 8;
-    if (per > 128) per = 128;
+    if (per > 64) per = 64;
     if (const char *env = getenv("PKV_DECODE_CHUNK_TILES")) {
         const int v = atoi(env);
         if (v >= 1 && v <= 4096) per = v;

@@ -12,22 +12,19 @@
 // Roles (320 threads):
 //   warps 0-3  softmax warpgroup of query head A, thread = query row = TMEM lane
 //   warps 4-7  softmax warpgroup of query head B
-//   warp 8     TMA producer: Q once, then K and V tiles of 64 keys through a
-//              3-stage ring (packed k/v: one box per half of head_dim; paged
-//              cache: one box per block segment, addressed via block_tables)
-//   warp 9     MMA issuer: iteration j issues S_j = Q K_j^T (M=128, N=64,
-//              K=head_dim) for both heads, then O += P_{j-1} V_{j-1}
-//              (M=128, N=head_dim, K=64), so the next scores are computed
-//              while the softmax warps work on the current ones
+//   warp 8     TMA producer: Q once, then K_0, V_0, K_1, ... (128 keys each)
+//              through a ring of kSlots tiles (packed k/v: one box per 64
+//              columns of head_dim; paged cache: one box per block segment,
+//              addressed via block_tables)
+//   warp 9     MMA issuer (one lane): S_A(0), S_B(0), then per key tile j
+//              P_A(j) V_j, S_A(j+1), P_B(j) V_j, S_B(j+1), so the tensor core
+//              works on one head while the other head's softmax runs
 //
-// Tensor memory (fp32 accumulators, lane = query row), 512 columns:
-//   S[head][buffer] at 64*(2*head+buffer), two buffers per head;
-//   O_A at 256, O_B at 256+d.
-// P is double-buffered per head in shared memory too: the softmax of tile j
-// writes buffer j%2, which the P V of tile j-2 has released.  Barrier
-// arrivals from the softmax warpgroups are one per warp.
+// Tensor memory (fp32 accumulators, lane = query row), 512 columns: S of
+// head t at 128 t (P, bf16 pairs, written over its first 64 columns and
+// read from there as the A operand of P V), O of head t at 256 + d t.
 //
-// Shared-memory operands use the 128-byte swizzle written by TMA: Q, K and P
+// Shared-memory operands use the 128-byte swizzle written by TMA: Q and K
 // are K-major, V is read as an MN-major B operand (keys are K, head_dim N).
 //
 // Softmax: per row, scores are scaled by scale*log2(e) and exponentiated
@@ -209,13 +206,6 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
 }
 
 // Wait that gives up when another role has aborted, or after the time bound

@@ -150,6 +150,25 @@ def kv_bytes(ctx: torch.Tensor, heads) -> int:
     return int(ctx.to(torch.int64).sum()) * heads.num_kv_heads * heads.head_dim * 2 * 2
 
 
+def pack_inputs(tensors):
+    """CPU tensors -> (pinned host byte buffer, device byte buffer, device views):
+    the step's inputs live in one buffer (parts 256-byte aligned), so that a
+    single copy moves all of them."""
+    offs, total = [], 0
+    for t in tensors:
+        total = (total + 255) // 256 * 256
+        offs.append(total)
+        total += t.numel() * t.element_size()
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for t, o in zip(tensors, offs):
+        n = t.numel() * t.element_size()
+        host[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8))
+    dev = host.cuda()
+    views = [dev[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+             for t, o in zip(tensors, offs)]
+    return host, dev, views
+
+
 class DecodeStep:
     """kv_build_decode_slots -> kv_store -> paged_attn_decode on resident
     inputs, or with fused=True the same step as paged_attn_decode_store (the
@@ -162,9 +181,11 @@ class DecodeStep:
         shape = (h.num_blocks, h.block_size, h.num_kv_heads, h.head_dim)
         self.kc = W.fill_normal_(torch.empty(shape, dtype=torch.bfloat16, device="cuda"), cache_seed)
         self.vc = W.fill_normal_(torch.empty(shape, dtype=torch.bfloat16, device="cuda"), cache_seed + 1)
-        self.q, self.k, self.v = (t.cuda() for t in (work.q, work.k, work.v))
-        self.bt = work.block_tables.cuda()
-        self.ctx = work.context_lens.cuda()
+        # q, the new k/v, block tables and context lengths: views of one
+        # device buffer (and its pinned host copy) so that the end-to-end
+        # measurement moves a step's inputs with one copy
+        self.inputs_host, self.inputs, (self.q, self.k, self.v, self.bt, self.ctx) = pack_inputs(
+            [work.q, work.k, work.v, work.block_tables, work.context_lens])
         self.slots = torch.empty(work.batch, dtype=torch.int32, device="cuda")
         self.out = torch.empty_like(self.q)
         self.max_ctx = work.max_context_len
@@ -339,20 +360,16 @@ def time_steps(step, steps: int, warmup: int, world: int, kernel_events=True, st
 # end to end through the C ABI with host buffers
 # ---------------------------------------------------------------------------
 def e2e_decode(step: DecodeStep, graph, steps: int, warmup: int, world: int):
-    """Every step copies its inputs (q, new k/v, context lengths, block tables)
-    from pinned host memory, runs the step (the captured graph of the public
-    API calls), and reads the output back to pinned host memory."""
-    w = step.work
-    host = {n: t.pin_memory() for n, t in (("q", w.q), ("k", w.k), ("v", w.v),
-                                           ("ctx", w.context_lens), ("bt", w.block_tables))}
-    dev = {"q": step.q, "k": step.k, "v": step.v, "ctx": step.ctx, "bt": step.bt}
+    """Every step copies its inputs (q, new k/v, block tables, context
+    lengths: one pinned host buffer, one copy) to the device, runs the step
+    (the captured graph of the public API calls), and reads the output back
+    to pinned host memory."""
     out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = step.inputs_host.numel()
     d2h = out_host.numel() * out_host.element_size()
 
     def one():
-        for n, t in host.items():
-            dev[n].copy_(t, non_blocking=True)
+        step.inputs.copy_(step.inputs_host, non_blocking=True)
         graph.replay()
         out_host.copy_(step.out, non_blocking=True)
 

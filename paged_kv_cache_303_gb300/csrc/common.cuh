@@ -154,6 +154,14 @@ __device__ __forceinline__ void st_v4(void *p, uint4 v) {
                  : "memory");
 }
 
+// store with the streaming (evict-first) cache hint: data written once and
+// not read again soon
+__device__ __forceinline__ void st_cs_v4(void *p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // three-input maximum (one instruction on sm_100 and later)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;

@@ -100,6 +100,9 @@ __global__ void __launch_bounds__(256) decode_slots_kernel(
 // D, both row strides and all four base pointers are multiples of 8 elements
 // (16 bytes) -- checked on the host.
 // ---------------------------------------------------------------------------
+#ifndef PKV_STORE_CS
+#define PKV_STORE_CS 1            // cache rows written with the streaming hint
+#endif
 constexpr int kStoreWarps = 8;
 constexpr int kStoreUnroll = 4;   // 16-byte vectors per lane per tensor per pass
 
@@ -135,8 +138,13 @@ __global__ void __launch_bounds__(kStoreWarps * 32) kv_store_v16_kernel(
         for (int u = 0; u < kStoreUnroll; ++u) {
             const int64_t e = base + u * kStep;
             if (e < D) {
-                st_v4(kdst + e, kr[u]);
-                st_v4(vdst + e, vr[u]);
+                if (PKV_STORE_CS) {
+                    st_cs_v4(kdst + e, kr[u]);
+                    st_cs_v4(vdst + e, vr[u]);
+                } else {
+                    st_v4(kdst + e, kr[u]);
+                    st_v4(vdst + e, vr[u]);
+                }
             }
         }
     }
@@ -374,15 +382,15 @@ qk_norm_rope_store_kernel(const __grid_constant__ PrologueParams p) {
                     st_v4(dst + ea, oA);
                     st_v4(dst + HALF + ea, oB);
                 }
-                if (dst2) {
-                    st_v4(dst2 + ea, oA);
-                    st_v4(dst2 + HALF + ea, oB);
+                if (dst2) {                     // cache row: streaming hint, as kv_store
+                    st_cs_v4(dst2 + ea, oA);
+                    st_cs_v4(dst2 + HALF + ea, oB);
                 }
             }
             if (!is_q && !is_k && r < rows && store) {
                 uint16_t *dst = p.vc + slot * D + (int64_t)(r - p.hq - p.hkv) * HD;
-                st_v4(dst + ea, xa[u]);
-                st_v4(dst + HALF + ea, xb[u]);
+                st_cs_v4(dst + ea, xa[u]);
+                st_cs_v4(dst + HALF + ea, xb[u]);
             }
         }
 

@@ -646,7 +646,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                             pkt.y = pack_bf16x2(o[v * 8 + 2] * inv, o[v * 8 + 3] * inv);
                             pkt.z = pack_bf16x2(o[v * 8 + 4] * inv, o[v * 8 + 5] * inv);
                             pkt.w = pack_bf16x2(o[v * 8 + 6] * inv, o[v * 8 + 7] * inv);
-                            *reinterpret_cast<uint4 *>(orow + cc * 32 + v * 8) = pkt;
+                            st_cs_v4(orow + cc * 32 + v * 8, pkt);   // written once
                         }
                     }
                 }

@@ -246,7 +246,9 @@ size_t paged_attn_prefill_workspace_size(int32_t num_seqs, int32_t total_q,
  *   max_context_len >= every context_lens[b] (host-side bound used to size
  *   the launch; a larger device value is clamped and flagged).
  * workspace: at least paged_attn_decode_workspace_size() bytes of device
- * scratch (NULL when that is 0); content need not be initialised.  Calls
+ * scratch (256 bytes or more for any batch > 0: it holds the counter from
+ * which the kernel's resident CTAs claim chunks, zeroed by the call in stream
+ * order, and the chunk partials); content need not be initialised.  Calls
  * that share a workspace must be ordered on the device.
  * Supported: head_dim 64 or 128; num_heads / num_kv_heads in {1,2,4,8};
  * block_size a power of two.
@@ -305,11 +307,12 @@ int paged_attn_decode_store(const pkv_bf16 *q, int64_t q_row_stride,
  * memory, such as a plugin inside a host framework that owns every device
  * allocation and only passes tensors in, or a runtime that forbids
  * allocations after start-up.  It computes exactly what paged_attn_decode
- * computes, with the same arguments minus the workspace: the split partials
- * go to a static device array of PKV_DECODE_STATIC_SCRATCH_BYTES owned by the
- * library, which every GPU that loads the library keeps resident until the
- * process exits.  The caller still passes inputs and outputs.  It calls no
- * cudaMalloc, cudaFree or allocating library routine.
+ * computes, with the same arguments minus the workspace: its scratch (the
+ * chunk counter and the split partials) goes to a static device array of
+ * PKV_DECODE_STATIC_SCRATCH_BYTES owned by the library, which every GPU
+ * that loads the library keeps resident until the process exits.  The
+ * caller still passes inputs and outputs.  It calls no cudaMalloc, cudaFree
+ * or allocating library routine.
  *   - A launch whose paged_attn_decode_workspace_size() exceeds
  *     PKV_DECODE_STATIC_SCRATCH_BYTES is rejected with PKV_ERR_WORKSPACE and
  *     a message saying so; nothing is launched.

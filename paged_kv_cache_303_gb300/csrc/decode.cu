@@ -3,9 +3,13 @@
 // the keys of a sequence split into chunks that are reduced independently
 // and merged by the online-softmax rescaling of §5.2.
 //
-// Work unit: one CTA per (kv head, chunk of keys, sequence).  The CTA holds
-// the GQA group's G query vectors (all query heads that share the kv head,
-// §3) in shared memory, so every K/V byte it reads serves G heads.
+// Work items: (chunk of keys, sequence, kv head).  A CTA works on one item
+// at a time with the GQA group's G query vectors (all query heads that share
+// the kv head, §3) in shared memory, so every K/V byte it reads serves G
+// heads.  The CTAs are persistent -- one resident wave, four per SM (128
+// registers a thread) -- and claim items from a counter in the workspace,
+// chunk index outermost, so the full chunks are taken before the short last
+// chunks of each sequence.
 //
 // Data path:
 //   * K and V of 32 tokens at a time ("tile") are staged into shared memory
@@ -13,12 +17,13 @@
 //     (box: 64 head_dim elements x 1 head x min(block_size, 32) slots).  With
 //     block_size >= 8 the boxes use the 128-byte swizzle so that the
 //     row-per-lane reads below are bank-conflict free.
-//   * One producer warp keeps a 3-stage ring full (an mbarrier pair per
-//     stage); three consumer warps each take whole tiles in turn, with no
-//     CTA-wide barrier inside the loop.  Four CTAs share an SM (128
-//     registers a thread), so that one CTA's start-up and merge overlap the
-//     others' streaming: more CTAs per SM beat a deeper ring here (3 stages
-//     x 4 CTAs 5.21 TB/s, 4 x 3 5.08, 6 x 2 4.26 on the batch-64 workload).
+//   * One producer warp claims items, writes each item's record and scaled
+//     query vectors into a two-entry item queue, and keeps a 3-stage tile
+//     ring full (an mbarrier pair per stage) across item boundaries, so the
+//     next item's first tiles are in flight while the consumers merge the
+//     current one.  Three consumer warps take the queue's items in order;
+//     tile i of an item goes to warp i % 3, with no CTA-wide barrier inside
+//     the tile loop.
 //   * Scores: lane = token; the lane dots its key row with the G queries
 //     (packed fp32x2 FMAs).  Scores carry scale*log2(e) so the softmax uses
 //     exp2.
@@ -29,17 +34,21 @@
 //     not complete (sequence tail, missing block) tokens whose probabilities
 //     are all zero are skipped, so garbage in unwritten cache slots never
 //     reaches the sum.
-//   * Fused store (paged_attn_decode_store): the CTA whose chunk holds
-//     position ctx-1 first writes the step's new K/V row of its kv head to
-//     that slot (the decode slot of Lesson 04 §4), with generic stores from
-//     the producer warp, then orders them before its TMA reads with a proxy
+//   * Fused store (paged_attn_decode_store): for the item whose chunk holds
+//     position ctx-1 the producer warp first writes the step's new K/V row
+//     of its kv head to that slot (the decode slot of Lesson 04 §4) with
+//     generic stores, then orders them before its TMA reads with a proxy
 //     fence; the tile that holds the new token then loads it like any other.
-//     Exactly one CTA per (sequence, kv head) writes; a padding row writes
+//     Exactly one item per (sequence, kv head) writes; a padding row writes
 //     nothing.
-//   * The consumer warps' (m, l, o) are merged once per chunk; a
-//     single-chunk launch writes bf16 out and lse directly, otherwise each CTA
-//     writes (m, l, unnormalised o) in fp32 to the workspace and
+//   * The consumer warps' (m, l, o) are merged in warp order at the end of
+//     each item (the result does not depend on which CTA took the item); a
+//     single-chunk launch writes bf16 out and lse directly, otherwise the
+//     item's (m, l, unnormalised o) go to the workspace in fp32 and
 //     decode_combine_kernel merges the chunks of each (sequence, head).
+//   * How it was reached (kernel GB/s, qwen3-decode-b64): one CTA per item
+//     with 3 stages x 4 CTAs/SM 5.21, 4 x 3 5.08, 6 x 2 4.26; the persistent
+//     form 5.33 (per-item start-up hidden behind the previous item).
 //
 // Bound: HBM.  Algorithmic bytes per launch = sum_b ctx_b * Hkv * d * 2 * 2
 // (K and V, bf16) + q and out; arithmetic intensity about G FLOP/byte.
@@ -104,25 +113,12 @@ struct DecodeParams {
     float *lse;
     float *part_o;             // [B, Hq, S, HD] fp32 (split mode)
     float *part_ml;            // [B, Hq, S, 2]  fp32 (split mode)
+    unsigned int *work_counter; // items handed out so far (zeroed before the launch)
+    int32_t batch;
     // fused store: this step's key/value rows [B, Hkv, HD] (null: no store)
     const uint16_t *new_k, *new_v;
     int64_t new_k_rs, new_v_rs;
     uint16_t *k_cache, *v_cache;
-};
-
-template <int HD, int G>
-struct Layout {
-    static constexpr int kHalves = HD / 64;                      // 128-byte rows per head_dim
-    static constexpr int kTileBytes = kHalves * kTile * 128;     // one of K or V
-    static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kPipeBytes = kStages * kStageBytes;
-    static constexpr int kOffBar = kPipeBytes;                   // full[S], empty[S], masks, abort
-    static constexpr int kOffQ = kOffBar + 256;                  // q, fp32 [G][HD]
-    static constexpr int kOffP = kOffQ + G * HD * 4;             // probabilities [warp][G][kTile]
-    static constexpr int kBytes = kOffP + kConsumers * G * kTile * 4;
-    // end-of-chunk merge buffers reuse the pipeline
-    static_assert(kConsumers * G * (HD + 2) * 4 <= kPipeBytes, "merge buffer must fit");
-    static_assert(kStages * 20 + 4 <= 256, "barrier area");
 };
 
 template <bool SW>
@@ -150,15 +146,43 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     }
 }
 
-// Roles: warps 0..kConsumers-1 consume tiles (tile i -> warp i % kConsumers,
-// stage i % kStages); warp kConsumers is the TMA producer.  A consumer warp
-// owns a whole tile: lane = token for the scores, lane = HD/32 head_dim
-// elements for P.V, and keeps its own (m, l, o) for the G heads; the warps'
-// states are merged once at the end of the chunk.
+// ---------------------------------------------------------------------------
+// The split kernel.  One resident wave of CTAs; the producer of each CTA
+// claims work items -- (chunk, sequence, kv head), chunk index outermost, so
+// the full chunks come before the short last chunks -- from a counter, loads
+// the item's G query vectors into a two-entry item queue in shared memory and
+// streams the item's tiles through the ring; consumers take the items from
+// the queue in order.  Tile i of an item goes to consumer warp i % kConsumers
+// and the warps' states are merged in warp order, so the result does not
+// depend on which CTA claimed which item.  The next item's query vectors and
+// first tiles are loaded while the consumers merge the current item.
+// ---------------------------------------------------------------------------
+constexpr int kQ = 2;                               // item queue entries
+
+struct ItemRec {
+    int b, kvh, split, tok_begin, tok_end, ntiles, pad0, pad1;
+};
+
+template <int HD, int G>
+struct Layout {
+    static constexpr int kHalves = HD / 64;
+    static constexpr int kTileBytes = kHalves * kTile * 128;
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kPipeBytes = kStages * kStageBytes;
+    static constexpr int kOffBar = kPipeBytes;      // full[S] empty[S] ready[Q] free[Q] masks abort
+    static constexpr int kOffItems = kOffBar + 256; // ItemRec[kQ], then two decision words
+    static constexpr int kOffQ = kOffItems + 128;   // q (scaled fp32) [kQ][G][HD]; merge buffer
+    static constexpr int kOffP = kOffQ + kQ * G * HD * 4;            // [warp][G][kTile]
+    static constexpr int kOffML = kOffP + kConsumers * G * kTile * 4; // [warp][G][2]
+    static constexpr int kBytes = kOffML + kConsumers * G * 2 * 4;
+    static_assert(2 * kStages * 8 + 2 * kQ * 8 + kStages * 4 + 4 <= 256, "barrier area");
+    static_assert(kQ * (int)sizeof(ItemRec) + 8 <= 128, "item area");
+};
+
 template <int HD, int G, bool SW>
 __global__ void __launch_bounds__(kThreads, PKV_DEC_MIN_CTAS)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
-                    const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
+                      const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
     using L = Layout<HD, G>;
     constexpr int DPL = HD / 32;                    // head_dim elements per lane in P.V
     constexpr int CPR = HD / 8;                     // 16-byte chunks per K row
@@ -169,344 +193,418 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     unsigned char *pipe = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
     uint64_t *empty = full + kStages;
-    uint32_t *seg_valid = reinterpret_cast<uint32_t *>(empty + kStages);   // [kStages]
+    uint64_t *ready = empty + kStages;              // [kQ] item entry written
+    uint64_t *freed = ready + kQ;                   // [kQ] item merged, entry reusable
+    uint32_t *seg_valid = reinterpret_cast<uint32_t *>(freed + kQ);   // [kStages]
     volatile int *abort_flag = reinterpret_cast<volatile int *>(seg_valid + kStages);
-    float *qs = reinterpret_cast<float *>(smem + L::kOffQ);
+    ItemRec *items = reinterpret_cast<ItemRec *>(smem + L::kOffItems);
+    // consumer-wide decisions, published by one thread before a barrier so
+    // that every consumer warp takes the same path through the barriers
+    int *decide = reinterpret_cast<int *>(smem + L::kOffItems + kQ * sizeof(ItemRec));
+    float *qring = reinterpret_cast<float *>(smem + L::kOffQ);
     float *ps = reinterpret_cast<float *>(smem + L::kOffP);
+    float *mml = reinterpret_cast<float *>(smem + L::kOffML);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int kvh = blockIdx.x;
-    const int split = blockIdx.y;
-    const int b = blockIdx.z;
-    const int hq0 = kvh * G;
     const bool direct = (p.max_splits == 1);
-
-    int ctx = p.ctx[b];
-    const bool ctx_ok = ctx >= 0 && ctx <= p.max_context_len;
-    if (!ctx_ok) {
-        if (tid == 0 && split == 0) atomicOr(&g_decode_status, PKV_STATUS_BAD_LENGTH);
-        ctx = ctx < 0 ? 0 : p.max_context_len;
-    }
-    const int tok_begin = split * p.chunk;
-    if (tok_begin >= ctx) {
-        // nothing to read; a padding row (ctx == 0) still owns its output
-        if (direct && split == 0) {
-            for (int i = tid; i < G * HD; i += kThreads) {
-                const int h = i / HD, e = i % HD;
-                p.out[(int64_t)b * p.out_rs + (int64_t)(hq0 + h) * HD + e] = 0;
-            }
-            if (p.lse && tid < G) p.lse[(int64_t)b * p.num_heads + hq0 + tid] = -INFINITY;
-        }
-        return;
-    }
-    const int tok_end = min(ctx, tok_begin + p.chunk);
-    const int ntiles = (tok_end - tok_begin + kTile - 1) / kTile;
-    const int32_t *bt_row = p.bt + (int64_t)b * p.bt_stride;
     const int bs = p.block_size;
     const int TB = bs < kTile ? bs : kTile;          // slots per TMA box
+    const int per_split = p.batch * p.num_kv_heads;
+    const int total = per_split * p.max_splits;
 
-    // TMA producer (one lane of the last warp): stage tile i into stage i % kStages
-    const uint32_t box_bytes = (uint32_t)TB * 128u;
-    auto issue = [&](int i, uint64_t policy) {
-        const int stage = i % kStages;
-        const int p0 = tok_begin + i * kTile;
-        const int nv = min(kTile, tok_end - p0);
-        const int nseg = (nv + TB - 1) / TB;
-        int ok = 0;
-        uint32_t mask = 0;               // bit sg: segment sg was loaded
-        for (int sg = 0; sg < nseg; ++sg) {
-            const int pos = p0 + sg * TB;
-            const int lb = pos / bs;
-            const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
-            if (blk >= 0 && blk < p.num_blocks) {
-                ++ok;
-                mask |= 1u << sg;
-            }
+    if (warp == kConsumers && lane == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
         }
-        // published to the consumers by the release of the arrive below
-        seg_valid[stage] = mask;
-        mbar_arrive_expect_tx(&full[stage], (uint32_t)ok * L::kHalves * 2u * box_bytes);
-        unsigned char *kdst = pipe + stage * L::kStageBytes;
-        unsigned char *vdst = kdst + L::kTileBytes;
-        for (int sg = 0; sg < nseg; ++sg) {
-            if (!((mask >> sg) & 1u)) {
-                atomicOr(&g_decode_status, PKV_STATUS_BAD_BLOCK);
-                continue;
-            }
-            const int pos = p0 + sg * TB;
-            const int blk = bt_row[pos / bs];
-            const int z = (int)((int64_t)blk * bs + pos % bs);
-#pragma unroll
-            for (int hf = 0; hf < L::kHalves; ++hf) {
-                const int off = hf * kTile * 128 + sg * TB * 128;
-                tma_load_3d(kdst + off, &kmap, &full[stage], hf * 64, kvh, z, policy);
-                tma_load_3d(vdst + off, &vmap, &full[stage], hf * 64, kvh, z, policy);
-            }
+        for (int e = 0; e < kQ; ++e) {
+            mbar_init(&ready[e], 1);
+            mbar_init(&freed[e], 1);
         }
-    };
-    const int prologue = ntiles < kStages ? ntiles : kStages;
-
-    if (warp == kConsumers) {
-        // fused store: the chunk that holds position ctx-1 writes the new
-        // token's row of this kv head before any tile is requested
-        if (p.new_k != nullptr && ctx_ok && ctx - 1 >= tok_begin && ctx - 1 < tok_end) {
-            const int pos = ctx - 1;
-            const int lb = pos / bs;
-            const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
-            if (blk >= 0 && blk < p.num_blocks) {
-                const int64_t dst = ((int64_t)blk * bs + pos % bs) * p.num_kv_heads * HD +
-                                    (int64_t)kvh * HD + lane * DPL;
-                const uint16_t *ks = p.new_k + (int64_t)b * p.new_k_rs + (int64_t)kvh * HD + lane * DPL;
-                const uint16_t *vs = p.new_v + (int64_t)b * p.new_v_rs + (int64_t)kvh * HD + lane * DPL;
-                if constexpr (DPL == 4) {
-                    const uint2 kw = *reinterpret_cast<const uint2 *>(ks);
-                    const uint2 vw = *reinterpret_cast<const uint2 *>(vs);
-                    *reinterpret_cast<uint2 *>(p.k_cache + dst) = kw;
-                    *reinterpret_cast<uint2 *>(p.v_cache + dst) = vw;
-                } else {
-                    const uint32_t kw = *reinterpret_cast<const uint32_t *>(ks);
-                    const uint32_t vw = *reinterpret_cast<const uint32_t *>(vs);
-                    *reinterpret_cast<uint32_t *>(p.k_cache + dst) = kw;
-                    *reinterpret_cast<uint32_t *>(p.v_cache + dst) = vw;
-                }
-                // the row is read back below by TMA (the async proxy)
-                fence_proxy_async_global();
-            }
-            __syncwarp();
-        }
-        // the producer starts the first kStages tiles before anything else,
-        // so that their latency overlaps the query load below
-        if (lane == 0) {
-            for (int s = 0; s < kStages; ++s) {
-                mbar_init(&full[s], 1);
-                mbar_init(&empty[s], 1);
-            }
-            *abort_flag = 0;
-            fence_barrier_init();
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
-            const uint64_t policy = policy_evict_first();
-            for (int i = 0; i < prologue; ++i) issue(i, policy);
-        }
-    } else {
-        // the G query vectors of this kv head, scaled by scale*log2(e), as fp32
-        for (int i = tid; i < G * HD / 8; i += kConsumers * 32) {
-            const int h = i / (HD / 8), c = i % (HD / 8);
-            const uint4 w = *reinterpret_cast<const uint4 *>(p.q + (int64_t)b * p.q_rs +
-                                                             (int64_t)(hq0 + h) * HD + c * 8);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-            float *dst = qs + h * HD + c * 8;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                dst[2 * k] = bf16lo_to_f32(ws[k]) * p.scale_log2;
-                dst[2 * k + 1] = bf16hi_to_f32(ws[k]) * p.scale_log2;
-            }
-        }
+        *abort_flag = 0;
+        fence_barrier_init();
     }
     __syncthreads();
 
     if (warp == kConsumers) {
+        // ------------------------------------------------------------------
+        // producer warp: claim items, fill the item queue, stream the tiles
+        // ------------------------------------------------------------------
         if (lane == 0) {
-            const uint64_t policy = policy_evict_first();
-            int issued = prologue;
-            for (int i = prologue; i < ntiles; ++i) {
-                const int stage = i % kStages;
-                if (!wait_or_abort(&empty[stage], (uint32_t)((i / kStages) - 1) & 1u, abort_flag))
-                    break;
-                issue(i, policy);
-                ++issued;
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
+        }
+        const uint64_t policy = policy_evict_first();
+        const uint32_t box_bytes = (uint32_t)TB * 128u;
+        int seq = 0, g = 0;
+        bool live = true;
+        while (live) {
+            int idx = 0;
+            if (lane == 0) idx = (int)atomicAdd(p.work_counter, 1u);
+            idx = __shfl_sync(0xffffffffu, idx, 0);
+            ItemRec it{};
+            const bool have = idx < total;
+            if (have) {
+                it.split = idx / per_split;
+                const int rem = idx % per_split;
+                it.b = rem / p.num_kv_heads;
+                it.kvh = rem % p.num_kv_heads;
+                int ctx = p.ctx[it.b];
+                if (ctx < 0 || ctx > p.max_context_len) {
+                    if (lane == 0 && it.split == 0 && it.kvh == 0)
+                        atomicOr(&g_decode_status, PKV_STATUS_BAD_LENGTH);
+                    ctx = ctx < 0 ? 0 : p.max_context_len;
+                }
+                it.tok_begin = it.split * p.chunk;
+                it.tok_end = min(ctx, it.tok_begin + p.chunk);
+                it.ntiles = it.tok_begin < ctx ? (it.tok_end - it.tok_begin + kTile - 1) / kTile : 0;
+                if (it.ntiles == 0) {
+                    // nothing to read; a padding row still owns its output
+                    if (direct && it.split == 0) {
+                        const int hq0 = it.kvh * G;
+                        for (int i = lane; i < G * HD; i += 32) {
+                            const int h = i / HD, e = i % HD;
+                            p.out[(int64_t)it.b * p.out_rs + (int64_t)(hq0 + h) * HD + e] = 0;
+                        }
+                        if (p.lse && lane < G) p.lse[(int64_t)it.b * p.num_heads + hq0 + lane] = -INFINITY;
+                    }
+                    continue;
+                }
+                // fused store: the chunk that holds position ctx-1 writes the
+                // new token's row of its kv head before requesting any tile
+                const bool ctx_ok = p.ctx[it.b] >= 0 && p.ctx[it.b] <= p.max_context_len;
+                if (p.new_k != nullptr && ctx_ok && ctx - 1 >= it.tok_begin && ctx - 1 < it.tok_end) {
+                    const int pos = ctx - 1;
+                    const int lb = pos / bs;
+                    const int32_t *bt_row = p.bt + (int64_t)it.b * p.bt_stride;
+                    const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
+                    if (blk >= 0 && blk < p.num_blocks) {
+                        const int64_t dst = ((int64_t)blk * bs + pos % bs) * p.num_kv_heads * HD +
+                                            (int64_t)it.kvh * HD + lane * DPL;
+                        const uint16_t *ks = p.new_k + (int64_t)it.b * p.new_k_rs + (int64_t)it.kvh * HD + lane * DPL;
+                        const uint16_t *vs = p.new_v + (int64_t)it.b * p.new_v_rs + (int64_t)it.kvh * HD + lane * DPL;
+                        if constexpr (DPL == 4) {
+                            *reinterpret_cast<uint2 *>(p.k_cache + dst) = *reinterpret_cast<const uint2 *>(ks);
+                            *reinterpret_cast<uint2 *>(p.v_cache + dst) = *reinterpret_cast<const uint2 *>(vs);
+                        } else {
+                            *reinterpret_cast<uint32_t *>(p.k_cache + dst) = *reinterpret_cast<const uint32_t *>(ks);
+                            *reinterpret_cast<uint32_t *>(p.v_cache + dst) = *reinterpret_cast<const uint32_t *>(vs);
+                        }
+                        // the row is read back below by TMA (the async proxy)
+                        fence_proxy_async_global();
+                    }
+                    __syncwarp();
+                }
             }
+            // the queue entry of this item was last used two items ago
+            const int e = seq % kQ;
+            bool ok = true;
+            if (lane == 0 && seq >= kQ) ok = wait_or_abort(&freed[e], (uint32_t)((seq / kQ) - 1) & 1u, abort_flag);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (!have) {
+                if (lane == 0) {
+                    items[e].ntiles = -1;               // end of the queue
+                    mbar_arrive(&ready[e]);
+                }
+                break;
+            }
+            // the item's G query vectors, scaled by scale*log2(e), as fp32
+            float *qd = qring + e * G * HD;
+            for (int c = lane; c < G * HD / 8; c += 32) {
+                const int h = c / (HD / 8), cc = c % (HD / 8);
+                const uint4 w = *reinterpret_cast<const uint4 *>(p.q + (int64_t)it.b * p.q_rs +
+                                                                 (int64_t)(it.kvh * G + h) * HD + cc * 8);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                float *dst = qd + h * HD + cc * 8;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    dst[2 * k] = bf16lo_to_f32(ws[k]) * p.scale_log2;
+                    dst[2 * k + 1] = bf16hi_to_f32(ws[k]) * p.scale_log2;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                items[e] = it;
+                mbar_arrive(&ready[e]);                 // releases q and the record
+                // the item's tiles, tile i -> ring position g
+                const int32_t *bt_row = p.bt + (int64_t)it.b * p.bt_stride;
+                for (int i = 0; i < it.ntiles; ++i, ++g) {
+                    const int stage = g % kStages;
+                    if (g >= kStages &&
+                        !wait_or_abort(&empty[stage], (uint32_t)((g / kStages) - 1) & 1u, abort_flag)) {
+                        live = false;
+                        break;
+                    }
+                    const int p0 = it.tok_begin + i * kTile;
+                    const int nv = min(kTile, it.tok_end - p0);
+                    const int nseg = (nv + TB - 1) / TB;
+                    int okc = 0;
+                    uint32_t mask = 0;                  // bit sg: segment sg was loaded
+                    for (int sg = 0; sg < nseg; ++sg) {
+                        const int pos = p0 + sg * TB;
+                        const int lb = pos / bs;
+                        const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
+                        if (blk >= 0 && blk < p.num_blocks) {
+                            ++okc;
+                            mask |= 1u << sg;
+                        }
+                    }
+                    seg_valid[stage] = mask;            // released by the arrive below
+                    mbar_arrive_expect_tx(&full[stage], (uint32_t)okc * L::kHalves * 2u * box_bytes);
+                    unsigned char *kdst = pipe + stage * L::kStageBytes;
+                    unsigned char *vdst = kdst + L::kTileBytes;
+                    for (int sg = 0; sg < nseg; ++sg) {
+                        if (!((mask >> sg) & 1u)) {
+                            atomicOr(&g_decode_status, PKV_STATUS_BAD_BLOCK);
+                            continue;
+                        }
+                        const int pos = p0 + sg * TB;
+                        const int blk = bt_row[pos / bs];
+                        const int z = (int)((int64_t)blk * bs + pos % bs);
+#pragma unroll
+                        for (int hf = 0; hf < L::kHalves; ++hf) {
+                            const int off = hf * kTile * 128 + sg * TB * 128;
+                            tma_load_3d(kdst + off, &kmap, &full[stage], hf * 64, it.kvh, z, policy);
+                            tma_load_3d(vdst + off, &vmap, &full[stage], hf * 64, it.kvh, z, policy);
+                        }
+                    }
+                }
+            }
+            live = __shfl_sync(0xffffffffu, live ? 1 : 0, 0) != 0;
+            ++seq;
+        }
+        if (lane == 0) {
             // no copy may still be landing when the CTA exits
-            for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+            for (int j = g > kStages ? g - kStages : 0; j < g; ++j)
                 (void)mbar_wait(&full[j % kStages], (uint32_t)(j / kStages) & 1u);
         }
         return;
     }
 
     // ----------------------------------------------------------------------
-    // consumer warps
+    // consumer warps: items in queue order
     // ----------------------------------------------------------------------
-    float m_run[G], l_part[G];
-    float2 o2[G][DPL / 2];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m_run[h] = -INFINITY;
-        l_part[h] = 0.f;
-#pragma unroll
-        for (int k = 0; k < DPL / 2; ++k) o2[h][k] = make_float2(0.f, 0.f);
-    }
     float *pw = ps + warp * G * kTile;             // this warp's probabilities [G][kTile]
-    // this lane's slice of a value row: head_dim elements [lane*DPL, lane*DPL+DPL)
     const int v_half = (lane * DPL) / 64;
     const int v_chunk = ((lane * DPL) % 64) / 8;
     const int v_byte = ((lane * DPL) % 8) * 2;
     const uint32_t all_segs = kTile / TB >= 32 ? 0xffffffffu : ((1u << (kTile / TB)) - 1u);
-
-    for (int i = warp; i < ntiles; i += kConsumers) {
-        const int stage = i % kStages;
-        if (!wait_or_abort(&full[stage], (uint32_t)(i / kStages) & 1u, abort_flag)) break;
-        const unsigned char *ktile = pipe + stage * L::kStageBytes;
-        const unsigned char *vtile = ktile + L::kTileBytes;
-        const int p0 = tok_begin + i * kTile;
-
-        // ---- scores: lane = token ----
-        float2 acc[G][2];
-#pragma unroll
-        for (int h = 0; h < G; ++h) acc[h][0] = acc[h][1] = make_float2(0.f, 0.f);
-#pragma unroll 4
-        for (int c = 0; c < CPR; ++c) {
-            const uint4 w = *reinterpret_cast<const uint4 *>(ktile + (c / 8) * kTile * 128 +
-                                                             chunk_off<SW>(lane, c % 8));
-            const float2 k0 = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
-            const float2 k1 = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
-            const float2 k2 = make_float2(bf16lo_to_f32(w.z), bf16hi_to_f32(w.z));
-            const float2 k3 = make_float2(bf16lo_to_f32(w.w), bf16hi_to_f32(w.w));
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float4 qa = *reinterpret_cast<const float4 *>(qs + h * HD + c * 8);
-                const float4 qb = *reinterpret_cast<const float4 *>(qs + h * HD + c * 8 + 4);
-                acc[h][0] = ffma2(make_float2(qa.x, qa.y), k0, acc[h][0]);
-                acc[h][1] = ffma2(make_float2(qa.z, qa.w), k1, acc[h][1]);
-                acc[h][0] = ffma2(make_float2(qb.x, qb.y), k2, acc[h][0]);
-                acc[h][1] = ffma2(make_float2(qb.z, qb.w), k3, acc[h][1]);
-            }
+    int g0 = 0;
+    for (int seq = 0;; ++seq) {
+        const int e = seq % kQ;
+        if (tid == 0) {
+            const bool ok = wait_or_abort(&ready[e], (uint32_t)(seq / kQ) & 1u, abort_flag);
+            decide[0] = ok ? 1 : 0;
         }
-        const uint32_t mask = seg_valid[stage];
-        const bool valid = (p0 + lane < tok_end) && ((mask >> (lane / TB)) & 1u);
-        // complete tile: every token present and loaded (warp-uniform)
-        const bool full_tile = (p0 + kTile <= tok_end) && mask == all_segs;
+        consumer_sync();
+        if (!decide[0]) break;                      // uniform
+        const ItemRec it = items[e];
+        if (it.ntiles < 0) break;                   // uniform
+        const float *qs = qring + e * G * HD;
+        const int hq0 = it.kvh * G;
 
-        // ---- online softmax over the warp's tile ----
-        float alpha[G];
+        float m_run[G], l_part[G];
+        float2 o2[G][DPL / 2];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const float s = valid ? (acc[h][0].x + acc[h][0].y) + (acc[h][1].x + acc[h][1].y)
-                                  : -INFINITY;
-            float mt = s;
+            m_run[h] = -INFINITY;
+            l_part[h] = 0.f;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-            const float m_new = fmaxf(m_run[h], mt);
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            alpha[h] = fast_exp2(m_run[h] - m_use);        // 0 while m_run is -inf
-            m_run[h] = m_new;
-            const float pr = fast_exp2(s - m_use);
-            l_part[h] = l_part[h] * alpha[h] + pr;
-            pw[h * kTile + lane] = pr;
+            for (int k = 0; k < DPL / 2; ++k) o2[h][k] = make_float2(0.f, 0.f);
         }
-        __syncwarp();
+        bool live = true;
+        for (int i = warp; i < it.ntiles; i += kConsumers) {
+            const int gt = g0 + i;
+            const int stage = gt % kStages;
+            if (!wait_or_abort(&full[stage], (uint32_t)(gt / kStages) & 1u, abort_flag)) {
+                live = false;
+                break;
+            }
+            const unsigned char *ktile = pipe + stage * L::kStageBytes;
+            const unsigned char *vtile = ktile + L::kTileBytes;
+            const int p0 = it.tok_begin + i * kTile;
 
-        // ---- P.V: lane = DPL head_dim elements ----
+            // ---- scores: lane = token ----
+            float2 acc[G][2];
 #pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int k = 0; k < DPL / 2; ++k) o2[h][k] = fmul2(o2[h][k], make_float2(alpha[h], alpha[h]));
-        const unsigned char *vrow0 = vtile + v_half * kTile * 128 + v_byte;
-        auto pv_token = [&](int t, const float (&pr)[G]) {
-            const unsigned char *src = vrow0 + chunk_off<SW>(t, v_chunk);
-            if constexpr (DPL == 4) {
-                const uint2 w = *reinterpret_cast<const uint2 *>(src);
-                const float2 v0 = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
-                const float2 v1 = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
+            for (int h = 0; h < G; ++h) acc[h][0] = acc[h][1] = make_float2(0.f, 0.f);
+#pragma unroll 4
+            for (int c = 0; c < CPR; ++c) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(ktile + (c / 8) * kTile * 128 +
+                                                                 chunk_off<SW>(lane, c % 8));
+                const float2 k0 = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
+                const float2 k1 = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
+                const float2 k2 = make_float2(bf16lo_to_f32(w.z), bf16hi_to_f32(w.z));
+                const float2 k3 = make_float2(bf16lo_to_f32(w.w), bf16hi_to_f32(w.w));
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    const float2 pp = make_float2(pr[h], pr[h]);
-                    o2[h][0] = ffma2(pp, v0, o2[h][0]);
-                    o2[h][1] = ffma2(pp, v1, o2[h][1]);
+                    const float4 qa = *reinterpret_cast<const float4 *>(qs + h * HD + c * 8);
+                    const float4 qb = *reinterpret_cast<const float4 *>(qs + h * HD + c * 8 + 4);
+                    acc[h][0] = ffma2(make_float2(qa.x, qa.y), k0, acc[h][0]);
+                    acc[h][1] = ffma2(make_float2(qa.z, qa.w), k1, acc[h][1]);
+                    acc[h][0] = ffma2(make_float2(qb.x, qb.y), k2, acc[h][0]);
+                    acc[h][1] = ffma2(make_float2(qb.z, qb.w), k3, acc[h][1]);
+                }
+            }
+            const uint32_t mask = seg_valid[stage];
+            const bool valid = (p0 + lane < it.tok_end) && ((mask >> (lane / TB)) & 1u);
+            const bool full_tile = (p0 + kTile <= it.tok_end) && mask == all_segs;
+
+            // ---- online softmax over the warp's tile ----
+            float alpha[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float s = valid ? (acc[h][0].x + acc[h][0].y) + (acc[h][1].x + acc[h][1].y)
+                                      : -INFINITY;
+                float mt = s;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+                const float m_new = fmaxf(m_run[h], mt);
+                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                alpha[h] = fast_exp2(m_run[h] - m_use);
+                m_run[h] = m_new;
+                const float pr = fast_exp2(s - m_use);
+                l_part[h] = l_part[h] * alpha[h] + pr;
+                pw[h * kTile + lane] = pr;
+            }
+            __syncwarp();
+
+            // ---- P.V: lane = DPL head_dim elements ----
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int k = 0; k < DPL / 2; ++k) o2[h][k] = fmul2(o2[h][k], make_float2(alpha[h], alpha[h]));
+            const unsigned char *vrow0 = vtile + v_half * kTile * 128 + v_byte;
+            auto pv_token = [&](int t, const float (&pr)[G]) {
+                const unsigned char *src = vrow0 + chunk_off<SW>(t, v_chunk);
+                if constexpr (DPL == 4) {
+                    const uint2 w = *reinterpret_cast<const uint2 *>(src);
+                    const float2 v0 = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
+                    const float2 v1 = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float2 pp = make_float2(pr[h], pr[h]);
+                        o2[h][0] = ffma2(pp, v0, o2[h][0]);
+                        o2[h][1] = ffma2(pp, v1, o2[h][1]);
+                    }
+                } else {
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
+                    const float2 v0 = make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w));
+#pragma unroll
+                    for (int h = 0; h < G; ++h) o2[h][0] = ffma2(make_float2(pr[h], pr[h]), v0, o2[h][0]);
+                }
+            };
+            if (full_tile) {
+#pragma unroll 2
+                for (int t4 = 0; t4 < kTile; t4 += 4) {
+                    float4 pq[G];
+#pragma unroll
+                    for (int h = 0; h < G; ++h) pq[h] = *reinterpret_cast<const float4 *>(pw + h * kTile + t4);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float pr[G];
+#pragma unroll
+                        for (int h = 0; h < G; ++h)
+                            pr[h] = u == 0 ? pq[h].x : u == 1 ? pq[h].y : u == 2 ? pq[h].z : pq[h].w;
+                        pv_token(t4 + u, pr);
+                    }
                 }
             } else {
-                const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
-                const float2 v0 = make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w));
-#pragma unroll
-                for (int h = 0; h < G; ++h) o2[h][0] = ffma2(make_float2(pr[h], pr[h]), v0, o2[h][0]);
-            }
-        };
-        if (full_tile) {
-#pragma unroll 2
-            for (int t4 = 0; t4 < kTile; t4 += 4) {
-                float4 pq[G];
-#pragma unroll
-                for (int h = 0; h < G; ++h) pq[h] = *reinterpret_cast<const float4 *>(pw + h * kTile + t4);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                // sequence tail or missing segment: skip tokens whose
+                // probabilities are all zero
+                for (int t = 0; t < kTile; ++t) {
                     float pr[G];
+                    bool any = false;
 #pragma unroll
-                    for (int h = 0; h < G; ++h)
-                        pr[h] = u == 0 ? pq[h].x : u == 1 ? pq[h].y : u == 2 ? pq[h].z : pq[h].w;
-                    pv_token(t4 + u, pr);
+                    for (int h = 0; h < G; ++h) {
+                        pr[h] = pw[h * kTile + t];
+                        any |= pr[h] != 0.f;
+                    }
+                    if (any) pv_token(t, pr);        // warp-uniform
                 }
             }
-        } else {
-            // sequence tail or missing segment: skip tokens whose
-            // probabilities are all zero, so rows that were not loaded (or
-            // hold unwritten cache slots) never reach the sum
-            for (int t = 0; t < kTile; ++t) {
-                float pr[G];
-                bool any = false;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+        }
+
+        // ---- merge the consumer warps' states, in warp order ----
+        // (the item's query vectors are no longer needed: their smem takes
+        // the merged output)
+        consumer_sync();
+        (void)live;
+        if (tid == 0) decide[1] = *abort_flag;      // read once, seen by all after the barrier
+        float *ob = const_cast<float *>(qs);            // [G][HD]
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float l = l_part[h];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+            if (lane == 0) {
+                mml[(warp * G + h) * 2] = m_run[h];
+                mml[(warp * G + h) * 2 + 1] = l;
+            }
+        }
+        consumer_sync();
+        const bool aborted = decide[1] != 0;        // uniform
+        float f_own[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float m = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) m = fmaxf(m, mml[(w * G + h) * 2]);
+            const float mu = (m == -INFINITY) ? 0.f : m;
+            f_own[h] = fast_exp2(m_run[h] - mu);
+        }
+#pragma unroll 1
+        for (int w = 0; w < kConsumers; ++w) {
+            if (warp == w) {
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    pr[h] = pw[h * kTile + t];
-                    any |= pr[h] != 0.f;
+                    float *dst = ob + h * HD + lane * DPL;
+#pragma unroll
+                    for (int k = 0; k < DPL / 2; ++k) {
+                        const float ox = f_own[h] * o2[h][k].x, oy = f_own[h] * o2[h][k].y;
+                        dst[2 * k] = (w == 0 ? 0.f : dst[2 * k]) + ox;
+                        dst[2 * k + 1] = (w == 0 ? 0.f : dst[2 * k + 1]) + oy;
+                    }
                 }
-                if (any) pv_token(t, pr);        // warp-uniform
+            }
+            consumer_sync();
+        }
+        for (int idx = tid; idx < G * HD && !aborted; idx += kConsumers * 32) {
+            const int h = idx / HD, ee = idx % HD;
+            float m = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) m = fmaxf(m, mml[(w * G + h) * 2]);
+            const float mu = (m == -INFINITY) ? 0.f : m;
+            float l = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w)
+                l += fast_exp2(mml[(w * G + h) * 2] - mu) * mml[(w * G + h) * 2 + 1];
+            const float o = ob[h * HD + ee];
+            const int hq = hq0 + h;
+            if (direct) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                p.out[(int64_t)it.b * p.out_rs + (int64_t)hq * HD + ee] =
+                    (uint16_t)(pack_bf16x2(o * inv, 0.f) & 0xffffu);
+                if (p.lse && ee == 0)
+                    p.lse[(int64_t)it.b * p.num_heads + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            } else {
+                const int64_t part = ((int64_t)it.b * p.num_heads + hq) * p.max_splits + it.split;
+                p.part_o[part * HD + ee] = o;
+                if (ee == 0) {
+                    p.part_ml[part * 2] = m;
+                    p.part_ml[part * 2 + 1] = l;
+                }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
-    }
-
-    // ---- merge the consumer warps' states ----
-    consumer_sync();                                   // every warp is done with the pipeline
-    const bool aborted = *abort_flag != 0;
-    float *mo = reinterpret_cast<float *>(pipe);       // [warp][G][HD]
-    float *mml = mo + kConsumers * G * HD;             // [warp][G][2]
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        float l = l_part[h];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-        if (lane == 0) {
-            mml[(warp * G + h) * 2] = m_run[h];
-            mml[(warp * G + h) * 2 + 1] = l;
-        }
-        float *dst = mo + (warp * G + h) * HD + lane * DPL;
-#pragma unroll
-        for (int k = 0; k < DPL / 2; ++k) {
-            dst[2 * k] = o2[h][k].x;
-            dst[2 * k + 1] = o2[h][k].y;
-        }
-    }
-    consumer_sync();
-    if (aborted) return;
-    for (int idx = tid; idx < G * HD; idx += kConsumers * 32) {
-        const int h = idx / HD, e = idx % HD;
-        float m = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) m = fmaxf(m, mml[(w * G + h) * 2]);
-        const float mu = (m == -INFINITY) ? 0.f : m;
-        float o = 0.f, l = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) {
-            const float f = fast_exp2(mml[(w * G + h) * 2] - mu);
-            l += f * mml[(w * G + h) * 2 + 1];
-            o += f * mo[(w * G + h) * HD + e];
-        }
-        const int hq = hq0 + h;
-        if (direct) {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            p.out[(int64_t)b * p.out_rs + (int64_t)hq * HD + e] =
-                (uint16_t)(pack_bf16x2(o * inv, 0.f) & 0xffffu);
-            if (p.lse && e == 0)
-                p.lse[(int64_t)b * p.num_heads + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-        } else {
-            const int64_t part = ((int64_t)b * p.num_heads + hq) * p.max_splits + split;
-            p.part_o[part * HD + e] = o;
-            if (e == 0) {
-                p.part_ml[part * 2] = m;
-                p.part_ml[part * 2 + 1] = l;
-            }
-        }
+        // the entry (record, q / merge buffer) may be refilled
+        consumer_sync();
+        if (tid == 0) mbar_arrive(&freed[e]);
+        if (aborted) break;                         // uniform, after the last barrier
+        g0 += it.ntiles;
     }
 }
 
@@ -554,15 +652,23 @@ int launch_split(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParam
     auto kern = decode_split_kernel<HD, G, SW>;
     const size_t smem = 1024 /*alignment slack*/ + Layout<HD, G>::kBytes;
     static bool configured[64];                        // per device
+    static int resident[64];                           // CTAs of this kernel per SM
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
     if (!configured[dev & 63]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
+        int nb = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, smem);
+        if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
+        resident[dev & 63] = nb > 0 ? nb : 1;
         configured[dev & 63] = true;
     }
-    dim3 grid(num_kv_heads, p.max_splits, batch);
+    // one resident wave; the CTAs claim the items
+    const int64_t items = (int64_t)batch * num_kv_heads * p.max_splits;
+    const int64_t wave = (int64_t)num_sms() * resident[dev & 63];
+    const dim3 grid((unsigned)(items < wave ? items : wave));
     kern<<<grid, kThreads, smem, stream>>>(km, vm, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
@@ -605,9 +711,11 @@ size_t decode_workspace_bytes(int32_t batch, int32_t num_heads, int32_t num_kv_h
                               int32_t head_dim, int32_t max_context_len) {
     int32_t chunk, splits;
     decode_plan(batch, num_kv_heads, head_dim, max_context_len, &chunk, &splits);
-    if (splits <= 1) return 0;
+    // a work counter (256 bytes, first), then the chunk partials
+    const size_t counter = 256;
+    if (splits <= 1) return counter;
     const size_t parts = (size_t)batch * num_heads * splits;
-    return parts * head_dim * sizeof(float) + parts * 2 * sizeof(float) + 256;
+    return counter + parts * head_dim * sizeof(float) + parts * 2 * sizeof(float) + 256;
 }
 
 int launch_decode(const DecodeArgs &a, cudaStream_t stream, const char **err) {
@@ -642,14 +750,21 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream, const char **err) {
     p.new_v_rs = a.new_v_rs;
     p.k_cache = const_cast<uint16_t *>(a.k_cache);
     p.v_cache = const_cast<uint16_t *>(a.v_cache);
+    p.batch = a.batch;
+    // workspace: the item counter (zeroed here, in stream order), then the
+    // chunk partials when there is more than one chunk
+    const size_t need = decode_workspace_bytes(a.batch, a.num_heads, a.num_kv_heads, a.head_dim,
+                                               a.max_context_len);
+    if (!a.workspace || a.workspace_bytes < need) {
+        *err = "paged_attn_decode: workspace smaller than paged_attn_decode_workspace_size()";
+        return PKV_ERR_WORKSPACE;
+    }
+    uintptr_t w = (reinterpret_cast<uintptr_t>(a.workspace) + 255) & ~uintptr_t(255);
+    p.work_counter = reinterpret_cast<unsigned int *>(w);
+    cudaError_t me = cudaMemsetAsync(p.work_counter, 0, sizeof(unsigned int), stream);
+    if (me != cudaSuccess) { *err = cudaGetErrorString(me); return PKV_ERR_CUDA; }
+    w += 256;
     if (splits > 1) {
-        const size_t need = decode_workspace_bytes(a.batch, a.num_heads, a.num_kv_heads,
-                                                   a.head_dim, a.max_context_len);
-        if (!a.workspace || a.workspace_bytes < need) {
-            *err = "paged_attn_decode: workspace smaller than paged_attn_decode_workspace_size()";
-            return PKV_ERR_WORKSPACE;
-        }
-        uintptr_t w = (reinterpret_cast<uintptr_t>(a.workspace) + 255) & ~uintptr_t(255);
         p.part_o = reinterpret_cast<float *>(w);
         p.part_ml = p.part_o + (size_t)a.batch * a.num_heads * splits * a.head_dim;
     }

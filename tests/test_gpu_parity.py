@@ -212,6 +212,7 @@ DECODE_SHAPES = [
     (8, 8, 128, 16, [33, 200, 511]),
     (16, 2, 128, 64, [65, 640, 1]),
     (8, 1, 64, 32, [300, 31, 32]),
+    (16, 8, 128, 16, [0, 5, 0, 200, 1]),      # one chunk per row, padding rows
 ]
 
 

@@ -21,7 +21,7 @@
 //              works on one head while the other head's softmax runs
 //
 // Tensor memory (fp32 accumulators, lane = query row), 512 columns: S of
-// head t at 128 t (P, bf16 pairs, written over its first 64 columns and
+// head t at 128 t (P, bf16 pairs, written over its upper 64 columns and
 // read from there as the A operand of P V), O of head t at 256 + d t.
 //
 // Shared-memory operands use the 128-byte swizzle written by TMA: Q and K
@@ -79,6 +79,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr int kCostBins = 2048;
+constexpr int kColP = kBN / 2;    // P (bf16 pairs) over the upper half of a head's S columns
 
 // ---------------------------------------------------------------------------
 // tcgen05 / tensor-memory wrappers
@@ -196,6 +197,30 @@ __device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t 
 }
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// One softmax pass over a row's 128 scores: p = 2^(s*sc - mu) as bf16 pairs
+// stored over the row's upper 64 S columns (not waited for), and the row sum
+// of p in acc.
+__device__ __forceinline__ void exp_pack_store(const uint32_t (&sr)[kBN], float sc, float mu,
+                                               uint32_t tS, float2 (&acc)[2]) {
+    const float2 sc2 = make_float2(sc, sc);
+    const float2 nm2 = make_float2(-mu, -mu);
+    acc[0] = acc[1] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int hpart = 0; hpart < 2; ++hpart) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const int col = hpart * 64 + 2 * c;
+            const float2 x = ffma2(make_float2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])),
+                                   sc2, nm2);
+            const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            acc[c & 1] = fadd2(acc[c & 1], e);
+            pk[c] = pack_bf16x2(e.x, e.y);
+        }
+        tmem_st32_nowait(tS + kColP + hpart * 32, pk);
+    }
 }
 
 // D (TMEM) += A (TMEM, K-major) * B (shared memory descriptor)
@@ -490,7 +515,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         auto issue_PV = [&](int j, int t) {
             const int s = (2 * j + 1) % kSlots;
             const uint64_t b0 = sdesc_sw128(ring + s * L::kKVTile, kBN * 128, 1024);
-            const uint32_t a_tm = tmem + L::kColS + t * kBN;           // P: kBN/2 columns
+            const uint32_t a_tm = tmem + L::kColS + t * kBN + kColP;   // P: kBN/2 columns
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
                 umma_bf16_ts(tmem + L::kColO + t * HD, a_tm + kk * 8, b0 + (uint32_t)((kk * 16 * 128) >> 4),
@@ -554,28 +579,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 live = wait_or_abort(&s_full[t], (uint32_t)j & 1u, abort_flag);
                 if (!__all_sync(0xffffffffu, live)) { live = false; break; }
                 tc_fence_after();
+                // scores of the tile, with the causal mask on the tiles that
+                // cross the row's bound
+                const int limit = off + qi - j * kBN;   // columns <= limit are visible
                 uint32_t sr[kBN];
                 tmem_ld128(tS, sr);
-                // row maximum of the raw scores (scale > 0), causal mask on the
-                // tiles that cross the row's bound
-                const int limit = off + qi - j * kBN;   // columns <= limit are visible
                 if (limit < kBN - 1) {
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
                         if (c > limit) sr[c] = __float_as_uint(-INFINITY);
                 }
-                // eight independent partial maxima keep the dependency chains
-                // short; three-input max takes two new scores per instruction
-                float pm[8];
+                // row maximum of the raw scores (scale > 0), in four
+                // independent partial maxima; three-input max takes two new
+                // scores per instruction
+                float pm[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) pm[i] = __uint_as_float(sr[i]);
+                for (int i = 0; i < 4; ++i)
+                    pm[i] = fmaxf(__uint_as_float(sr[i]), __uint_as_float(sr[4 + i]));
 #pragma unroll
-                for (int c = 8; c < kBN; c += 16)
+                for (int c = 8; c < kBN; c += 8)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        pm[i] = fmax3(pm[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
-                const float rmax = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
-                                         fmaxf(pm[6], pm[7]));
+                    for (int i = 0; i < 4; ++i)
+                        pm[i] = fmax3(pm[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 4 + i]));
+                const float rmax = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
                 const float m_new = fmaxf(m, rmax * sc);
                 const bool rescale = (m == -INFINITY) ? (m_new != -INFINITY)
                                                       : (m_new > m + kRescaleThreshold);
@@ -585,9 +611,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     m = m_new;
                 }
                 const float mu = (m == -INFINITY) ? 0.f : m;
+                const bool any_rescale = __any_sync(0xffffffffu, rescale);
+                // p = 2^(s*scale - m), bf16 pairs written over the upper S columns
+                float2 acc[2];
+                exp_pack_store(sr, sc, mu, tS, acc);
                 // S_t(j) follows P_t(j-1) V_{j-1} on the tensor core, so O is
                 // final for the earlier tiles: rescale it in place if needed
-                if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                if (j > 0 && any_rescale) {
 #pragma unroll 1
                     for (int cc = 0; cc < HD / 32; ++cc) {
                         float o[32];
@@ -598,29 +628,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     }
                 }
                 l *= alpha;
-                // p = 2^(s*scale - m), bf16 pairs written over the S columns
-                const float2 sc2 = make_float2(sc, sc);
-                const float2 nm2 = make_float2(-mu, -mu);
-                float2 acc[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int hpart = 0; hpart < 2; ++hpart) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int col = hpart * 64 + 2 * c;
-                        const float2 x = ffma2(make_float2(__uint_as_float(sr[col]),
-                                                           __uint_as_float(sr[col + 1])), sc2, nm2);
-                        const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                        acc[c & 3] = fadd2(acc[c & 3], e);
-                        pk[c] = pack_bf16x2(e.x, e.y);
-                    }
-                    tmem_st32_nowait(tS + hpart * 32, pk);
-                }
                 tmem_wait_st();
-                l += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-                     ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+                l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[t]);

@@ -331,8 +331,24 @@ def test_decode_large_padded_sampled():
 # ---------------------------------------------------------------------------
 # prefill
 # ---------------------------------------------------------------------------
-def _prefill_packed(heads, lens, seed, fused=False):
+def _growing_scores(work, heads, rate=12.0):
+    """Make a row's scores rise along the keys: q[..., 0] is 0, 4 or 8 by row
+    (all three kinds in every warp) and k[..., 0] grows with the key's position
+    among the step's new tokens, so that rows with q[..., 0] = 8 see their
+    scores (log2 units of the softmax) rise by about `rate` per 128 keys and
+    move the running maximum past any lazy-rescale threshold on most tiles,
+    rows with 4 on some tiles, rows with 0 never."""
+    per_key = rate / 128 / (8 * heads.scale * math.log2(math.e))
+    pos = torch.cat([torch.arange(n) for n in work.q_lens.tolist()]).double()
+    work.k[:, :, 0] = (pos * per_key).to(torch.bfloat16)[:, None]
+    a = torch.tensor([0.0, 4.0, 8.0], dtype=torch.bfloat16)
+    work.q[:, :, 0] = a[torch.arange(work.q.shape[0]) % 3][:, None]
+
+
+def _prefill_packed(heads, lens, seed, fused=False, growing=False):
     work = W.prefill_work(heads, lens, seed=seed)
+    if growing:
+        _growing_scores(work, heads)
     ref, ref_lse = oracle.prefill(bits(work.q), bits(work.k), bits(work.v), work.cu_seqlens_q,
                                   work.cu_seqlens_k, heads.scale)
     if fused:
@@ -372,8 +388,10 @@ def test_prefill_fused_qkv_views():
     _prefill_packed(W.Heads(16, 8, 128, 16, 256), [300, 77], seed=650, fused=True)
 
 
-def _prefill_paged(heads, q_lens, prefix, seed, poison=True):
+def _prefill_paged(heads, q_lens, prefix, seed, poison=True, growing=False):
     work = W.prefill_work(heads, q_lens, prefix, seed=seed)
+    if growing:
+        _growing_scores(work, heads)
     kc, vc = W.history_cache(heads, seed + 1)
     if poison:
         _poison_unused(kc, vc, work.block_tables, work.prefix_lens)   # the chunk is written below
@@ -397,6 +415,15 @@ def _prefill_paged(heads, q_lens, prefix, seed, poison=True):
     assert np.array_equal(gs.cpu().numpy(), slots)
     assert_close(out, ref, "paged prefill out")
     assert np.allclose(lse.cpu().double().numpy(), ref_lse, atol=2e-3, rtol=1e-4)
+
+
+def test_prefill_growing_scores_move_the_running_maximum():
+    _prefill_packed(W.Heads(16, 8, 128, 16, 256), [700, 300, 129], seed=660, growing=True)
+
+
+def test_prefill_prefix_cache_growing_scores():
+    heads = W.Heads(16, 8, 128, 64, 96 * 4)
+    _prefill_paged(heads, [600, 200], [3 * 64, 64 + 5], seed=670, growing=True)
 
 
 @pytest.mark.parametrize("bs", [16, 64, 256])

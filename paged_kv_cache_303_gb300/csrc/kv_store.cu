@@ -103,6 +103,9 @@ __global__ void __launch_bounds__(256) decode_slots_kernel(
 #ifndef PKV_STORE_CS
 #define PKV_STORE_CS 1            // cache rows written with the streaming hint
 #endif
+#ifndef PKV_STORE_EARLY
+#define PKV_STORE_EARLY 1         // row loads issued before the slot is known
+#endif
 constexpr int kStoreWarps = 8;
 constexpr int kStoreUnroll = 4;   // 16-byte vectors per lane per tensor per pass
 
@@ -113,19 +116,13 @@ __global__ void __launch_bounds__(kStoreWarps * 32) kv_store_v16_kernel(
     const int32_t tok = blockIdx.x * kStoreWarps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (tok >= n) return;
-    const int64_t slot = slots[tok];
-    if (slot == -1) return;                     // padding token: leave the cache alone
-    if (slot < 0 || slot >= num_slots) {
-        if (lane == 0) flag(PKV_STATUS_BAD_SLOT);
-        return;
-    }
     const uint16_t *ksrc = key + (int64_t)tok * key_rs;
     const uint16_t *vsrc = value + (int64_t)tok * value_rs;
-    uint16_t *kdst = kc + slot * D;
-    uint16_t *vdst = vc + slot * D;
     constexpr int64_t kStep = 32 * 8;           // elements per warp-wide vector pass
-    for (int64_t base = (int64_t)lane * 8; base < D; base += kStep * kStoreUnroll) {
-        uint4 kr[kStoreUnroll], vr[kStoreUnroll];
+    // The first pass's row loads go out together with the slot load (they do
+    // not depend on it), so a token costs one memory round trip, not two.
+    uint4 kr[kStoreUnroll], vr[kStoreUnroll];
+    auto load_pass = [&](int64_t base) {
 #pragma unroll
         for (int u = 0; u < kStoreUnroll; ++u) {
             const int64_t e = base + u * kStep;
@@ -134,6 +131,18 @@ __global__ void __launch_bounds__(kStoreWarps * 32) kv_store_v16_kernel(
                 vr[u] = ld_stream_v4(vsrc + e);
             }
         }
+    };
+    if (PKV_STORE_EARLY) load_pass((int64_t)lane * 8);
+    const int64_t slot = slots[tok];
+    if (slot == -1) return;                     // padding token: leave the cache alone
+    if (slot < 0 || slot >= num_slots) {
+        if (lane == 0) flag(PKV_STATUS_BAD_SLOT);
+        return;
+    }
+    uint16_t *kdst = kc + slot * D;
+    uint16_t *vdst = vc + slot * D;
+    for (int64_t base = (int64_t)lane * 8; base < D; base += kStep * kStoreUnroll) {
+        if (!PKV_STORE_EARLY || base != (int64_t)lane * 8) load_pass(base);
 #pragma unroll
         for (int u = 0; u < kStoreUnroll; ++u) {
             const int64_t e = base + u * kStep;
@@ -187,15 +196,16 @@ __global__ void __launch_bounds__(kStoreWarps * 32) kv_store_scalar_kernel(
 // Work unit: one warp takes kProUnroll warp-wide passes of one token's rows
 // (a pass covers 32/(d/16) rows): 12 rows at head_dim 128, so a Qwen3 token
 // (16 q + 8 k + 8 v rows) is three units.  One resident wave of CTAs; each
-// warp walks its units and issues all loads of the next unit before
-// computing the current one, so two units' loads are in flight per warp.
+// warp walks its units with kProStages of them in flight: their rows are
+// copied into the warp's shared-memory stages by cp.async, so the loads
+// hold no registers while a unit is computed.
 // The unit's (cos, sin) of the d/2 pair angles are computed two per lane
 // and handed to the lanes that need them by shuffles.  The angle pos * f_i
 // is formed as pos * f_hi + (error of that product + pos * f_lo) with
 // f_hi + f_lo = theta^(-2i/d) computed on the host in double, so the angle
-// carries no fp32 rounding of f_i or of the product; sincosf of the rounded
-// part is then corrected to first order by the rest.  Value rows are copied
-// as they are.
+// carries no fp32 rounding of f_i or of the product; it is reduced by 2*pi
+// (Cody and Waite) and finished by the hardware sine / cosine.  Value rows
+// are copied as they are.
 // HBM-bound: per token it reads (Hq + 2*Hkv) * d * 2 bytes and writes
 // (Hq + 2*Hkv) * d * 2 bytes (+ Hkv * d * 2 when k is also written back).
 // ---------------------------------------------------------------------------
@@ -205,7 +215,13 @@ __global__ void __launch_bounds__(kStoreWarps * 32) kv_store_scalar_kernel(
 #ifndef PKV_PRO_MIN_CTAS
 #define PKV_PRO_MIN_CTAS 2
 #endif
-constexpr int kProWarps = 8;
+#ifndef PKV_PRO_STAGES
+#define PKV_PRO_STAGES 2      // units in flight per warp
+#endif
+#ifndef PKV_PRO_WARPS
+#define PKV_PRO_WARPS 8       // warps per CTA
+#endif
+constexpr int kProWarps = PKV_PRO_WARPS;
 constexpr int kProUnroll = PKV_PRO_UNROLL;
 
 struct PrologueParams {
@@ -241,169 +257,235 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
     return make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w));
 }
 
+// cos and sin of the angle ah + al (al: the rounding error of ah and the
+// low part of the frequency).  Cody and Waite's additive range reduction
+// with 2*pi split in two floats: k*P1 is subtracted exactly (ah and k*P1 are
+// multiples of 2^-22 once |ah| >= pi and the difference is below 4), k*P2
+// with one rounding, then al is added to the small remainder; the hardware
+// sine and cosine (absolute error about 2^-21 on [-pi, pi]) finish it.  The
+// split leaves 7e-15 * k of 2*pi unaccounted, 2e-8 rad at positions near 2^24.
+__device__ __forceinline__ void rope_cos_sin(float ah, float al, float &c, float &s) {
+    constexpr float kInv2Pi = 0x1.45f306p-3f;   // 1 / (2 pi), rounded to float
+    constexpr float kP1 = 0x1.921fb6p+2f;       // 2 pi rounded to float
+    constexpr float kP2 = -0x1.777a5cp-23f;     // 2 pi - kP1, rounded to float
+    const float k = rintf(ah * kInv2Pi);
+    float r = fmaf(-k, kP1, ah);
+    r = fmaf(-k, kP2, r) + al;
+    __sincosf(r, &s, &c);
+}
+
+// Norm, rotation and stores of one work unit whose rows are in xa / xb
+// (this lane's two 16-byte pieces of each pass).
 template <int HD>
-__global__ void __launch_bounds__(kProWarps * 32, PKV_PRO_MIN_CTAS)
-qk_norm_rope_store_kernel(const __grid_constant__ PrologueParams p) {
+__device__ __forceinline__ void prologue_unit(const PrologueParams &p, int64_t unit, int lane,
+                                              const uint4 (&xa)[kProUnroll],
+                                              const uint4 (&xb)[kProUnroll], int64_t slot, float pos,
+                                              uint4 wqa, uint4 wqb, uint4 wka, uint4 wkb) {
     constexpr int HALF = HD / 2;
     constexpr int LPR = HD / 16;                // lanes per row
     constexpr int RPW = 32 / LPR;               // rows per warp-wide pass
-    const int lane = threadIdx.x & 31;
     const int sub = lane / LPR;
-    // this lane's elements: ea .. ea+7 and their rotation partners ea+d/2 ..,
-    // so pair i = ea + j is (element i, element i + d/2) in one lane
+    const int ea = (lane % LPR) * 8;
+    const int rows = p.hq + 2 * p.hkv;
+    const int64_t D = (int64_t)p.hkv * HD;
+    const int64_t t = unit / p.chunks;
+    const int r0 = (int)(unit % p.chunks) * (RPW * kProUnroll);
+    const bool store = slot >= 0 && slot < p.num_slots;
+    if (lane == 0 && r0 == 0 && !store && slot != -1) flag(PKV_STATUS_BAD_SLOT);
+
+    float cs[8], sn[8];
+    if (r0 < p.hq + p.hkv) {                    // the unit rotates rows (warp-uniform)
+        // pairs 2*lane and 2*lane+1 (mod d/2) of the angle table
+        float c2[2], s2[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = (2 * lane + h) % HALF;
+            const float fh = p.inv_hi[i], fl = p.inv_lo[i];
+            const float ah = pos * fh;
+            const float al = fmaf(pos, fl, fmaf(pos, fh, -ah));
+            rope_cos_sin(ah, al, c2[h], s2[h]);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int src = ea / 2 + jj;        // lane holding pairs ea + 2jj, ea + 2jj + 1
+            cs[2 * jj] = __shfl_sync(0xffffffffu, c2[0], src);
+            cs[2 * jj + 1] = __shfl_sync(0xffffffffu, c2[1], src);
+            sn[2 * jj] = __shfl_sync(0xffffffffu, s2[0], src);
+            sn[2 * jj + 1] = __shfl_sync(0xffffffffu, s2[1], src);
+        }
+    }
+
+#pragma unroll
+    for (int u = 0; u < kProUnroll; ++u) {
+        const int r = r0 + u * RPW + sub;
+        const bool is_q = r < p.hq;
+        const bool is_k = !is_q && r < p.hq + p.hkv;
+        if (r0 + u * RPW < p.hq + p.hkv) {      // some row of this pass rotates (warp-uniform)
+            const uint32_t av[4] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w};
+            const uint32_t bv[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+            float2 fa[4], fb[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                fa[j] = unpack_bf16x2(av[j]);
+                fb[j] = unpack_bf16x2(bv[j]);
+            }
+            // every lane takes part in the shuffles, whatever its row is
+            float2 ss2 = fmul2(fa[0], fa[0]);
+#pragma unroll
+            for (int j = 1; j < 4; ++j) ss2 = ffma2(fa[j], fa[j], ss2);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ss2 = ffma2(fb[j], fb[j], ss2);
+            float ss = ss2.x + ss2.y;
+#pragma unroll
+            for (int off = LPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = rsqrtf(ss * (1.f / HD) + p.eps);
+            const float2 inv2 = make_float2(inv, inv);
+            const uint4 wa = is_q ? wqa : wka, wb = is_q ? wqb : wkb;
+            const uint32_t wav[4] = {wa.x, wa.y, wa.z, wa.w}, wbv[4] = {wb.x, wb.y, wb.z, wb.w};
+            uint32_t oa[4], ob[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                // y = bf16(bf16(x * inv) * w), the two roundings of the norm
+                const float2 na2 = fmul2(fa[j], inv2), nb2 = fmul2(fb[j], inv2);
+                const float2 ya = unpack_bf16x2(mul_bf16x2(pack_bf16x2(na2.x, na2.y), wav[j]));
+                const float2 yb = unpack_bf16x2(mul_bf16x2(pack_bf16x2(nb2.x, nb2.y), wbv[j]));
+                const float2 c = make_float2(cs[2 * j], cs[2 * j + 1]);
+                const float2 sv = make_float2(sn[2 * j], sn[2 * j + 1]);
+                // first half: y cos - partner sin; second half: y cos + partner sin
+                const float2 ra = ffma2(yb, make_float2(-sv.x, -sv.y), fmul2(ya, c));
+                const float2 rb = ffma2(ya, sv, fmul2(yb, c));
+                oa[j] = pack_bf16x2(ra.x, ra.y);
+                ob[j] = pack_bf16x2(rb.x, rb.y);
+            }
+            const uint4 oA = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+            const uint4 oB = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+            uint16_t *dst = nullptr, *dst2 = nullptr;
+            if (is_q) {
+                dst = p.q_out + t * p.q_out_rs + (int64_t)r * HD;
+            } else if (is_k) {
+                const int h = r - p.hq;
+                if (p.k_out) dst = p.k_out + t * p.k_out_rs + (int64_t)h * HD;
+                if (store) dst2 = p.kc + slot * D + (int64_t)h * HD;
+            }
+            if (dst) {
+                st_v4(dst + ea, oA);
+                st_v4(dst + HALF + ea, oB);
+            }
+            if (dst2) {                         // cache row: streaming hint, as kv_store
+                st_cs_v4(dst2 + ea, oA);
+                st_cs_v4(dst2 + HALF + ea, oB);
+            }
+        }
+        if (!is_q && !is_k && r < rows && store) {
+            uint16_t *dst = p.vc + slot * D + (int64_t)(r - p.hq - p.hkv) * HD;
+            st_cs_v4(dst + ea, xa[u]);
+            st_cs_v4(dst + HALF + ea, xb[u]);
+        }
+    }
+}
+
+// source row of pass u of a unit for this lane, or null past the last row
+template <int HD>
+__device__ __forceinline__ const uint16_t *prologue_row(const PrologueParams &p, int64_t t, int r) {
+    if (r < p.hq) return p.q + t * p.q_rs + (int64_t)r * HD;
+    if (r < p.hq + p.hkv) return p.k + t * p.k_rs + (int64_t)(r - p.hq) * HD;
+    if (r < p.hq + 2 * p.hkv) return p.v + t * p.v_rs + (int64_t)(r - p.hq - p.hkv) * HD;
+    return nullptr;
+}
+
+// Each warp keeps kProStages units in flight with cp.async (16-byte pieces,
+// zero-filled past the last row, plus the token's slot and position).
+constexpr int kProStages = PKV_PRO_STAGES;
+template <int HD>
+struct ProStage {
+    static constexpr int kPieceBytes = 32 * 16;                    // one piece of a pass, all lanes
+    static constexpr int kRowBytes = 2 * kProUnroll * kPieceBytes; // the unit's rows
+    static constexpr int kBytes = kRowBytes + 16;                  // + slot (4 B) and position (8 B)
+    static constexpr int kWarpBytes = kProStages * kBytes;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int HD>
+__global__ void __launch_bounds__(kProWarps * 32, PKV_PRO_MIN_CTAS)
+qk_norm_rope_store_kernel(const __grid_constant__ PrologueParams p) {
+    using S = ProStage<HD>;
+    constexpr int HALF = HD / 2;
+    constexpr int LPR = HD / 16;
+    constexpr int RPW = 32 / LPR;
+    extern __shared__ __align__(16) unsigned char pro_smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int sub = lane / LPR;
     const int ea = (lane % LPR) * 8;
     const int64_t total = (int64_t)p.n * p.chunks;
     const int64_t stride = (int64_t)gridDim.x * kProWarps;
-    int64_t unit = (int64_t)blockIdx.x * kProWarps + (threadIdx.x >> 5);
+    int64_t unit = (int64_t)blockIdx.x * kProWarps + warp;
     if (unit >= total) return;                  // uniform per warp
-    const int rows = p.hq + 2 * p.hkv;
-    const int64_t D = (int64_t)p.hkv * HD;
-    // both norms' weights for this lane's elements, packed bf16
     const uint4 wqa = ld_stream_v4(p.qw + ea), wqb = ld_stream_v4(p.qw + HALF + ea);
     const uint4 wka = ld_stream_v4(p.kw + ea), wkb = ld_stream_v4(p.kw + HALF + ea);
+    unsigned char *wbase = pro_smem + warp * S::kWarpBytes;
+    const uint32_t wbase_s = smem_u32(wbase);
 
-    // start the loads of a unit: its kProUnroll passes of rows, slot and position
-    auto load = [&](int64_t u_id, uint4 (&xa)[kProUnroll], uint4 (&xb)[kProUnroll],
-                    int64_t &slot, float &pos) {
-        const int64_t t = u_id / p.chunks;
-        const int r0 = (int)(u_id % p.chunks) * (RPW * kProUnroll);
+    // start the copies of unit u_id into stage st (one commit group per unit,
+    // also when there is no such unit, so that group counting stays uniform)
+    auto issue = [&](int64_t u_id, int st) {
+        if (u_id < total) {
+            const int64_t t = u_id / p.chunks;
+            const int r0 = (int)(u_id % p.chunks) * (RPW * kProUnroll);
+            const uint32_t sb = wbase_s + st * S::kBytes;
 #pragma unroll
-        for (int u = 0; u < kProUnroll; ++u) {
-            const int r = r0 + u * RPW + sub;
-            const uint16_t *src = nullptr;
-            if (r < p.hq)
-                src = p.q + t * p.q_rs + (int64_t)r * HD;
-            else if (r < p.hq + p.hkv)
-                src = p.k + t * p.k_rs + (int64_t)(r - p.hq) * HD;
-            else if (r < rows)
-                src = p.v + t * p.v_rs + (int64_t)(r - p.hq - p.hkv) * HD;
-            xa[u] = src ? ld_stream_v4(src + ea) : make_uint4(0u, 0u, 0u, 0u);
-            xb[u] = src ? ld_stream_v4(src + HALF + ea) : make_uint4(0u, 0u, 0u, 0u);
+            for (int u = 0; u < kProUnroll; ++u) {
+                const uint16_t *src = prologue_row<HD>(p, t, r0 + u * RPW + sub);
+                const uint32_t nbytes = src ? 16u : 0u;
+                const uint16_t *s0 = src ? src + ea : p.qw;
+                const uint16_t *s1 = src ? src + HALF + ea : p.qw;
+                cp_async16(sb + (2 * u) * S::kPieceBytes + lane * 16, s0, nbytes);
+                cp_async16(sb + (2 * u + 1) * S::kPieceBytes + lane * 16, s1, nbytes);
+            }
+            if (lane == 0) {
+                cp_async4(sb + S::kRowBytes, p.slots + t);
+                cp_async8(sb + S::kRowBytes + 8, p.pos + t);
+            }
         }
-        slot = p.slots[t];
-        pos = r0 < p.hq + p.hkv ? (float)p.pos[t] : 0.f;   // exact for positions below 2^24
+        cp_async_commit();
     };
 
-    uint4 xa[kProUnroll], xb[kProUnroll];
-    int64_t slot;
-    float pos;
-    load(unit, xa, xb, slot, pos);
-    for (;;) {
-        // the next unit's loads are in flight while this one is computed
-        const int64_t next = unit + stride;
-        uint4 na[kProUnroll], nb[kProUnroll];
-        int64_t slot_n = -1;
-        float pos_n = 0.f;
-        if (next < total) load(next, na, nb, slot_n, pos_n);
-
-        const int64_t t = unit / p.chunks;
+#pragma unroll
+    for (int k = 0; k < kProStages; ++k) issue(unit + k * stride, k);
+    int st = 0;
+    for (; unit < total; unit += stride) {
+        cp_async_wait<kProStages - 1>();       // this lane's copies of the unit have landed
+        __syncwarp();                           // ... and lane 0's slot / position
+        const unsigned char *sp = wbase + st * S::kBytes;
+        uint4 xa[kProUnroll], xb[kProUnroll];
+#pragma unroll
+        for (int u = 0; u < kProUnroll; ++u) {
+            xa[u] = *reinterpret_cast<const uint4 *>(sp + (2 * u) * S::kPieceBytes + lane * 16);
+            xb[u] = *reinterpret_cast<const uint4 *>(sp + (2 * u + 1) * S::kPieceBytes + lane * 16);
+        }
+        const int64_t slot = *reinterpret_cast<const int32_t *>(sp + S::kRowBytes);
+        const int64_t pos64 = *reinterpret_cast<const int64_t *>(sp + S::kRowBytes + 8);
+        __syncwarp();                           // every lane has read the stage before it is refilled
+        issue(unit + kProStages * stride, st);
         const int r0 = (int)(unit % p.chunks) * (RPW * kProUnroll);
-        const bool store = slot >= 0 && slot < p.num_slots;
-        if (lane == 0 && r0 == 0 && !store && slot != -1) flag(PKV_STATUS_BAD_SLOT);
-
-        float cs[8], sn[8];
-        if (r0 < p.hq + p.hkv) {                // the unit rotates rows (warp-uniform)
-            // pairs 2*lane and 2*lane+1 (mod d/2) of the angle table
-            float c2[2], s2[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int i = (2 * lane + h) % HALF;
-                const float fh = p.inv_hi[i], fl = p.inv_lo[i];
-                const float ah = pos * fh;
-                const float al = fmaf(pos, fl, fmaf(pos, fh, -ah));
-                float s0, c0;
-                sincosf(ah, &s0, &c0);
-                s2[h] = fmaf(al, c0, s0);
-                c2[h] = fmaf(-al, s0, c0);
-            }
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int src = ea / 2 + jj;    // lane holding pairs ea + 2jj, ea + 2jj + 1
-                cs[2 * jj] = __shfl_sync(0xffffffffu, c2[0], src);
-                cs[2 * jj + 1] = __shfl_sync(0xffffffffu, c2[1], src);
-                sn[2 * jj] = __shfl_sync(0xffffffffu, s2[0], src);
-                sn[2 * jj + 1] = __shfl_sync(0xffffffffu, s2[1], src);
-            }
-        }
-
-#pragma unroll
-        for (int u = 0; u < kProUnroll; ++u) {
-            const int r = r0 + u * RPW + sub;
-            const bool is_q = r < p.hq;
-            const bool is_k = !is_q && r < p.hq + p.hkv;
-            if (r0 + u * RPW < p.hq + p.hkv) {  // some row of this pass rotates (warp-uniform)
-                const uint32_t av[4] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w};
-                const uint32_t bv[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
-                float2 fa[4], fb[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    fa[j] = unpack_bf16x2(av[j]);
-                    fb[j] = unpack_bf16x2(bv[j]);
-                }
-                // every lane takes part in the shuffles, whatever its row is
-                float2 ss2 = fmul2(fa[0], fa[0]);
-#pragma unroll
-                for (int j = 1; j < 4; ++j) ss2 = ffma2(fa[j], fa[j], ss2);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) ss2 = ffma2(fb[j], fb[j], ss2);
-                float ss = ss2.x + ss2.y;
-#pragma unroll
-                for (int off = LPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                const float inv = rsqrtf(ss * (1.f / HD) + p.eps);
-                const float2 inv2 = make_float2(inv, inv);
-                const uint4 wa = is_q ? wqa : wka, wb = is_q ? wqb : wkb;
-                const uint32_t wav[4] = {wa.x, wa.y, wa.z, wa.w}, wbv[4] = {wb.x, wb.y, wb.z, wb.w};
-                uint32_t oa[4], ob[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    // y = bf16(bf16(x * inv) * w), the two roundings of the norm
-                    const float2 na2 = fmul2(fa[j], inv2), nb2 = fmul2(fb[j], inv2);
-                    const float2 ya = unpack_bf16x2(mul_bf16x2(pack_bf16x2(na2.x, na2.y), wav[j]));
-                    const float2 yb = unpack_bf16x2(mul_bf16x2(pack_bf16x2(nb2.x, nb2.y), wbv[j]));
-                    const float2 c = make_float2(cs[2 * j], cs[2 * j + 1]);
-                    const float2 sv = make_float2(sn[2 * j], sn[2 * j + 1]);
-                    // first half: y cos - partner sin; second half: y cos + partner sin
-                    const float2 ra = ffma2(yb, make_float2(-sv.x, -sv.y), fmul2(ya, c));
-                    const float2 rb = ffma2(ya, sv, fmul2(yb, c));
-                    oa[j] = pack_bf16x2(ra.x, ra.y);
-                    ob[j] = pack_bf16x2(rb.x, rb.y);
-                }
-                const uint4 oA = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-                const uint4 oB = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-                uint16_t *dst = nullptr, *dst2 = nullptr;
-                if (is_q) {
-                    dst = p.q_out + t * p.q_out_rs + (int64_t)r * HD;
-                } else if (is_k) {
-                    const int h = r - p.hq;
-                    if (p.k_out) dst = p.k_out + t * p.k_out_rs + (int64_t)h * HD;
-                    if (store) dst2 = p.kc + slot * D + (int64_t)h * HD;
-                }
-                if (dst) {
-                    st_v4(dst + ea, oA);
-                    st_v4(dst + HALF + ea, oB);
-                }
-                if (dst2) {                     // cache row: streaming hint, as kv_store
-                    st_cs_v4(dst2 + ea, oA);
-                    st_cs_v4(dst2 + HALF + ea, oB);
-                }
-            }
-            if (!is_q && !is_k && r < rows && store) {
-                uint16_t *dst = p.vc + slot * D + (int64_t)(r - p.hq - p.hkv) * HD;
-                st_cs_v4(dst + ea, xa[u]);
-                st_cs_v4(dst + HALF + ea, xb[u]);
-            }
-        }
-
-        if (next >= total) break;
-        unit = next;
-#pragma unroll
-        for (int u = 0; u < kProUnroll; ++u) {
-            xa[u] = na[u];
-            xb[u] = nb[u];
-        }
-        slot = slot_n;
-        pos = pos_n;
+        const float pos = r0 < p.hq + p.hkv ? (float)pos64 : 0.f;   // exact below 2^24
+        prologue_unit<HD>(p, unit, lane, xa, xb, slot, pos, wqa, wqb, wka, wkb);
+        st = st + 1 == kProStages ? 0 : st + 1;
     }
+    cp_async_wait<0>();                         // no copy may land after the warp has left
 }
 
 cudaError_t launch_qk_norm_rope_store(const PrologueArgs &a, cudaStream_t stream) {
@@ -444,10 +526,24 @@ cudaError_t launch_qk_norm_rope_store(const PrologueArgs &a, cudaStream_t stream
     const int64_t need = (units + kProWarps - 1) / kProWarps;
     const int64_t wave = (int64_t)num_sms() * PKV_PRO_MIN_CTAS;
     const dim3 grid((unsigned)(need < wave ? need : wave));
+    const int smem = kProWarps * (a.head_dim == 128 ? ProStage<128>::kWarpBytes : ProStage<64>::kWarpBytes);
+    static bool configured[64];                 // per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (!configured[dev & 63]) {
+        e = cudaFuncSetAttribute(qk_norm_rope_store_kernel<128>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kProWarps * ProStage<128>::kWarpBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(qk_norm_rope_store_kernel<64>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kProWarps * ProStage<64>::kWarpBytes);
+        if (e != cudaSuccess) return e;
+        configured[dev & 63] = true;
+    }
     if (a.head_dim == 128)
-        qk_norm_rope_store_kernel<128><<<grid, kProWarps * 32, 0, stream>>>(p);
+        qk_norm_rope_store_kernel<128><<<grid, kProWarps * 32, smem, stream>>>(p);
     else
-        qk_norm_rope_store_kernel<64><<<grid, kProWarps * 32, 0, stream>>>(p);
+        qk_norm_rope_store_kernel<64><<<grid, kProWarps * 32, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -128,6 +128,28 @@ def test_prologue_vs_oracle(hq, hkv, d, n, theta):
     _check_cache(gk, gv, slots, bits(k_out), bits(qkv[:, hq + hkv:]), num_slots)
 
 
+@pytest.mark.parametrize("hq,hkv,d,theta", [(16, 8, 128, 1e6), (4, 2, 64, 1e4)])
+def test_prologue_large_positions(hq, hkv, d, theta):
+    """Positions up to 2^24 - 1 (the largest the fp32 position is exact for):
+    angles of up to 1.7e7 rad must still be reduced accurately."""
+    n, bs = 200, 16
+    nb = (n + 40) // bs + 2
+    num_slots = nb * bs
+    qkv, pos, qw, kw, slots = _inputs(n, hq, hkv, d, seed=950 + d, num_slots=num_slots,
+                                      max_pos=2 ** 24 - 1)
+    pos[1] = 2 ** 24 - 1
+    ref_q, ref_k = _oracle(qkv, pos, qw, kw, hq, hkv, 1e-6, theta)
+    g = dev(qkv)
+    gk, gv = _canary_cache(nb, bs, hkv, d)
+    q_out, k_out = ops.qk_norm_rope_store(g[:, :hq], g[:, hq:hq + hkv], g[:, hq + hkv:], dev(pos),
+                                          dev(qw), dev(kw), gk, gv, dev(slots), 1e-6, theta,
+                                          k_out=torch.empty((n, hkv, d), dtype=torch.bfloat16,
+                                                            device="cuda"))
+    torch.cuda.synchronize()
+    assert_rotated_close(q_out, ref_q, "rotated q, large positions")
+    assert_rotated_close(k_out, ref_k, "rotated k, large positions")
+
+
 def test_prologue_in_place_equals_out_of_place():
     hq, hkv, d, n = 16, 8, 128, 200
     num_slots = 16 * 16

@@ -276,41 +276,47 @@ __device__ __forceinline__ int kv_tiles_for(int Lq, int Lk, int mb) {
 }
 
 // Work list: every (sequence, 128-row block), ordered by decreasing number
-// of key tiles (a counting sort on the cost).  One CTA.
+// of key tiles (a counting sort on the cost).  One CTA: a warp per sequence,
+// lanes over its row blocks; the scan runs over the bins in use only.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int32_t *work_count,
                                                             int2 *work) {
     __shared__ int hist[kCostBins];
-    __shared__ int total;
+    __shared__ int top;                         // highest cost bin in use
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     for (int i = threadIdx.x; i < kCostBins; i += blockDim.x) hist[i] = 0;
+    if (threadIdx.x == 0) top = 0;
     __syncthreads();
-    for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
+    for (int s = warp; s < p.num_seqs; s += nwarps) {
         const int Lq = p.cu_q[s + 1] - p.cu_q[s];
         const int Lk = p.cu_k[s + 1] - p.cu_k[s];
         if (Lq <= 0) continue;
-        if (Lk < Lq) { atomicOr(&g_prefill_status, PKV_STATUS_BAD_LENGTH); continue; }
+        if (Lk < Lq) {
+            if (lane == 0) atomicOr(&g_prefill_status, PKV_STATUS_BAD_LENGTH);
+            continue;
+        }
         const int nmb = (Lq + kBM - 1) / kBM;
-        for (int mb = 0; mb < nmb; ++mb)
+        for (int mb = lane; mb < nmb; mb += 32)
             atomicAdd(&hist[min(kv_tiles_for(Lq, Lk, mb), kCostBins - 1)], 1);
+        if (lane == 0) atomicMax(&top, min(kv_tiles_for(Lq, Lk, nmb - 1), kCostBins - 1));
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         int run = 0;   // descending cost: bins from high to low
-        for (int c = kCostBins - 1; c >= 0; --c) {
+        for (int c = top; c >= 0; --c) {
             const int h = hist[c];
             hist[c] = run;
             run += h;
         }
-        total = min(run, p.max_items);
         if (run > p.max_items) atomicOr(&g_prefill_status, PKV_STATUS_BAD_LENGTH);
-        *work_count = total;
+        *work_count = min(run, p.max_items);
     }
     __syncthreads();
-    for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
+    for (int s = warp; s < p.num_seqs; s += nwarps) {
         const int Lq = p.cu_q[s + 1] - p.cu_q[s];
         const int Lk = p.cu_k[s + 1] - p.cu_k[s];
         if (Lq <= 0 || Lk < Lq) continue;
         const int nmb = (Lq + kBM - 1) / kBM;
-        for (int mb = 0; mb < nmb; ++mb) {
+        for (int mb = lane; mb < nmb; mb += 32) {
             const int pos = atomicAdd(&hist[min(kv_tiles_for(Lq, Lk, mb), kCostBins - 1)], 1);
             if (pos < p.max_items) work[pos] = make_int2(s, mb);
         }

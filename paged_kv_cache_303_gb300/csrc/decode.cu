@@ -21,9 +21,9 @@
 //     query vectors into a two-entry item queue, and keeps a 3-stage tile
 //     ring full (an mbarrier pair per stage) across item boundaries, so the
 //     next item's first tiles are in flight while the consumers merge the
-//     current one.  Three consumer warps take the queue's items in order;
-//     tile i of an item goes to warp i % 3, with no CTA-wide barrier inside
-//     the tile loop.
+//     current one.  Two consumer warps (kConsumers) take the queue's items
+//     in order; tile i of an item goes to warp i % kConsumers, with no
+//     CTA-wide barrier inside the tile loop.
 //   * Scores: lane = token; the lane dots its key row with the G queries
 //     (packed fp32x2 FMAs).  Scores carry scale*log2(e) so the softmax uses
 //     exp2.
@@ -48,7 +48,10 @@
 //     decode_combine_kernel merges the chunks of each (sequence, head).
 //   * How it was reached (kernel GB/s, qwen3-decode-b64): one CTA per item
 //     with 3 stages x 4 CTAs/SM 5.21, 4 x 3 5.08, 6 x 2 4.26; the persistent
-//     form 5.33 (per-item start-up hidden behind the previous item).
+//     form 5.33 (per-item start-up hidden behind the previous item); on it,
+//     two consumer warps per CTA instead of three (cheaper merges, more
+//     CTAs' producers in flight) 5.36 -> 5.52, and 4.93 -> 5.08 on the
+//     large batch-256 workload.
 //
 // Bound: HBM.  Algorithmic bytes per launch = sum_b ctx_b * Hkv * d * 2 * 2
 // (K and V, bf16) + q and out; arithmetic intensity about G FLOP/byte.
@@ -82,18 +85,23 @@ namespace {
 
 // Tunables (compile-time): consumer warps per CTA, ring depth, CTAs per SM.
 #ifndef PKV_DEC_CONSUMERS
-#define PKV_DEC_CONSUMERS 3
+#define PKV_DEC_CONSUMERS 2
 #endif
 #ifndef PKV_DEC_STAGES
 #define PKV_DEC_STAGES 3
 #endif
 #ifndef PKV_DEC_MIN_CTAS
-#define PKV_DEC_MIN_CTAS 4
+#define PKV_DEC_MIN_CTAS 5
 #endif
 constexpr int kConsumers = PKV_DEC_CONSUMERS;    // consumer warps per CTA
 constexpr int kThreads = (kConsumers + 1) * 32;  // + one TMA producer warp
 constexpr int kTile = 32;                        // tokens per pipeline stage (one per lane)
 constexpr int kStages = PKV_DEC_STAGES;
+// Consumer warp w takes tiles w, w + kConsumers, ... of the ring and waits on
+// the stage's full barrier by phase parity; with more warps than stages two
+// warps would wait on one stage for phases two apart, and the later one's
+// parity check would pass before its tile has landed.
+static_assert(kConsumers <= kStages, "one ring stage per consumer warp at least");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

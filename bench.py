@@ -426,7 +426,7 @@ def e2e_decode(step: DecodeStep, graph, steps: int, warmup: int, world: int):
     torch.cuda.synchronize()
     barrier(world)
     total = max_over_ranks(start.elapsed_time(end), world)
-    return total, h2d, d2h
+    return total, h2d, d2h, out_host
 
 
 # ---------------------------------------------------------------------------
@@ -539,7 +539,7 @@ def run_ours(args, rank, world):
     eager_achieved = dec_alg / (eager_dec_ms / 1e3) / 1e9
 
     # end to end, host buffers
-    e2e_ms, h2d, d2h = e2e_decode(dec, graph, args.steps, args.warmup, world)
+    e2e_ms, h2d, d2h, _ = e2e_decode(dec, graph, args.steps, args.warmup, world)
     e2e_val = dec.bytes * world * args.steps / (e2e_ms / 1e3) / 1e9
     dec_bytes = dec.bytes
     dec_launches = dec.launches

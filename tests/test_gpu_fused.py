@@ -229,3 +229,28 @@ def test_chunk_merge_with_dirty_workspace_twice(fused, monkeypatch):
         assert np.allclose(got[fin], ref_lse[fin], atol=2e-3, rtol=1e-4)
         outs.append(out.clone())
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_pipelined_end_to_end_steps_read_back_the_decode_output():
+    """The benchmark's end-to-end decode: two buffer sets on one cache, with
+    the host-to-device copies, the graph replays and the read-backs on three
+    streams.  Every step has the same inputs (the same new row is rewritten),
+    so each read-back must hold the oracle's output for the cache the step
+    read; the second buffer set shares the cache and not the inputs."""
+    import bench
+    work = W.decode_work(W.Heads(16, 8, 128, 16, 256), [40, 0, 300, 17, 129], seed=431)
+    h = work.heads
+    st = bench.DecodeStep(work, cache_seed=432, fused=True)
+    kref, vref = bits(st.kc.cpu()).copy(), bits(st.vc.cpu()).copy()   # before any step
+    slots = oracle.decode_slots(work.block_tables, work.context_lens, h.block_size)
+    oracle.kv_store(bits(work.k), bits(work.v), kref, vref, slots)
+    ref, _ = oracle.decode(bits(work.q), kref, vref, work.block_tables, work.context_lens, h.scale)
+    graph = st.capture()
+    _, h2d, d2h, out_host = bench.e2e_decode(st, graph, steps=5, warmup=2, world=1)
+    torch.cuda.synchronize()
+    assert h2d == st.inputs_host.numel() and d2h == st.out.numel() * st.out.element_size()
+    for b, oh in enumerate(out_host):
+        assert_close(oh, ref, f"read-back of buffer set {b}")
+        assert torch.equal(oh, st.out.cpu())
+    tw = st.twin()
+    assert tw.kc.data_ptr() == st.kc.data_ptr() and tw.inputs.data_ptr() != st.inputs.data_ptr()

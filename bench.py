@@ -39,6 +39,9 @@ METRIC = "paged-attn decode KV-read GB/s, prefill TFLOP/s, store_kvcache GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+NOMINAL_HBM_GBS = 7900.0      # HBM3e data-sheet bandwidth of one GB300 (context for the fraction)
+
+
 def peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -662,6 +665,7 @@ def run_ours(args, rank, world):
         "gpu_launches": dec_launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(dec_achieved, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(dec_achieved / hbm, 4), "traffic": traffic,
+                     "frac_of_nominal": round(dec_achieved / NOMINAL_HBM_GBS, 4),
                      "kernel": "paged_attn_decode_store (split kernel + merge kernel)",
                      "kernel_ms": round(dec_ms, 4),
                      "timing": "CUDA events around each replay of the captured decode call "

@@ -227,6 +227,21 @@ def test_decode_vs_oracle(shape, chunk_tiles, monkeypatch):
     _decode_case(heads, ctx, seed=300 + hq + d + bs)
 
 
+@pytest.mark.parametrize("bs", [1, 2, 8, 128])
+def test_decode_other_block_sizes(bs):
+    """Block sizes the decode shapes above leave out: one or two slots per
+    TMA box (no swizzle), 8 (the smallest swizzled box) and 128."""
+    ctx = [1, bs, bs + 1, 3 * bs + 5, 97, 0]
+    need = sum((c + bs - 1) // bs for c in ctx) + 3
+    _decode_case(W.Heads(16, 4, 128, bs, need), ctx, seed=340 + bs)
+
+
+@pytest.mark.parametrize("bs", [8, 128])
+def test_prefill_prefix_cache_other_block_sizes(bs):
+    heads = W.Heads(16, 8, 128, bs, 96 * 256 // bs)
+    _prefill_paged(heads, [100, 257, 7], [bs + 5, 3, 2 * bs], seed=790 + bs)
+
+
 def test_decode_tiny_pipeline():
     """Config 'tiny': slot mapping + store of the two prompts, then one decode
     step per sequence (new tokens at positions 6 and 3)."""

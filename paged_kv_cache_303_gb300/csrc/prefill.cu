@@ -42,7 +42,9 @@
 // unwritten cache slots (possibly NaN) never meet a zero probability.
 //
 // A one-CTA planning kernel lists the (sequence, 128-row block) work items
-// in decreasing order of key tiles (longest first) in the workspace.
+// in decreasing order of key tiles (longest first) in the workspace; the
+// prefill kernel is its programmatic dependent and reads the list after
+// griddepcontrol.wait, its set-up overlapping the planning.
 #include <math.h>
 
 #include "common.cuh"
@@ -79,7 +81,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr int kCostBins = 2048;
-constexpr int kColP = kBN / 2;    // P (bf16 pairs) over the upper half of a head's S columns
+constexpr int kColP = kBN / 2;
+#ifndef PKV_PF_PDL
+#define PKV_PF_PDL 1   // prefill kernel launched as a programmatic dependent of the planning kernel
+#endif    // P (bf16 pairs) over the upper half of a head's S columns
 
 // ---------------------------------------------------------------------------
 // tcgen05 / tensor-memory wrappers
@@ -282,6 +287,11 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int
                                                             int2 *work) {
     __shared__ int hist[kCostBins];
     __shared__ int top;                         // highest cost bin in use
+#if PKV_PF_PDL
+    // the prefill kernel may start its set-up now; it waits for this grid
+    // (and its writes) before reading the work list
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     for (int i = threadIdx.x; i < kCostBins; i += blockDim.x) hist[i] = 0;
     if (threadIdx.x == 0) top = 0;
@@ -347,22 +357,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int item = blockIdx.y;
-    if (item >= p.max_items || item >= *p.work_count) return;     // uniform for the CTA
-    const int2 w = p.work[item];
-    const int seq = w.x, mb = w.y;
-    const int q0 = p.cu_q[seq];
-    const int Lq = p.cu_q[seq + 1] - q0;
-    const int k0 = p.cu_k[seq];
-    const int Lk = p.cu_k[seq + 1] - k0;
-    const int off = Lk - Lq;
-    const int r0 = mb * kBM;
-    const int n_kv = kv_tiles_for(Lq, Lk, mb);
-    const int G = p.num_heads / p.num_kv_heads;
-    const int ntile = G >= 2 ? 2 : 1;
-    const int h0 = blockIdx.x * ntile;
-    const int kvh = h0 / G;
-
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
     uint64_t *q_full = bars + 0;
     uint64_t *slot_full = q_full + 1;          // [kSlots] a K or V tile landed
@@ -399,10 +393,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         *abort_flag = 0;
         fence_barrier_init();
     }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tensormap(&qmap);
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+#if PKV_PF_PDL
+    // the work list is written by the planning kernel launched just before
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+    const int item = blockIdx.y;
+    const bool idle = item >= p.max_items || item >= *p.work_count;     // uniform for the CTA
+    const int2 w = idle ? make_int2(0, 0) : p.work[item];
+    const int seq = w.x, mb = w.y;
+    const int q0 = idle ? 0 : p.cu_q[seq];
+    const int Lq = idle ? 1 : p.cu_q[seq + 1] - q0;
+    const int k0 = idle ? 0 : p.cu_k[seq];
+    const int Lk = idle ? 1 : p.cu_k[seq + 1] - k0;
+    const int off = Lk - Lq;
+    const int r0 = mb * kBM;
+    const int n_kv = kv_tiles_for(Lq, Lk, mb);
+    const int G = p.num_heads / p.num_kv_heads;
+    const int ntile = G >= 2 ? 2 : 1;
+    const int h0 = blockIdx.x * ntile;
+    const int kvh = h0 / G;
+
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (idle) {                                  // no work item for this CTA
+        if (warp == kMmaWarp) tmem_dealloc(tmem, L::kTmemCols);
+        return;
+    }
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------------
@@ -412,9 +435,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         bool issued_all = false;
         int issued_n = 0;
         if (lane == 0) {
-            prefetch_tensormap(&qmap);
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
             const uint64_t pol_stream = policy_evict_first();
             mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * L::kQTile));
             for (int t = 0; t < ntile; ++t)
@@ -714,9 +734,18 @@ int launch_hd(const PrefillArgs &a, const PrefillParams &pp, int2 *work, int32_t
     }
     const int G = a.num_heads / a.num_kv_heads;
     const int ntile = G >= 2 ? 2 : 1;
-    dim3 grid(a.num_heads / ntile, max_items);
-    kern<<<grid, kThreads, smem, stream>>>(qm, km, vm, pp);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_heads / ntile, max_items);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = PKV_PF_PDL ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, qm, km, vm, pp);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
     return PKV_OK;
 }

@@ -106,7 +106,10 @@ __global__ void __launch_bounds__(256) decode_slots_kernel(
 #ifndef PKV_STORE_EARLY
 #define PKV_STORE_EARLY 1         // row loads issued before the slot is known
 #endif
-constexpr int kStoreWarps = 8;
+#ifndef PKV_STORE_WARPS
+#define PKV_STORE_WARPS 8         // tokens (warps) per CTA
+#endif
+constexpr int kStoreWarps = PKV_STORE_WARPS;
 constexpr int kStoreUnroll = 4;   // 16-byte vectors per lane per tensor per pass
 
 __global__ void __launch_bounds__(kStoreWarps * 32) kv_store_v16_kernel(

@@ -346,7 +346,7 @@ class PrefillStep:
 
 def time_steps(step, steps: int, warmup: int, world: int, kernel_events=True, store_events=False):
     """Warm up, then time exactly `steps` steps between barriers/synchronizes.
-    Returns (total ms over ranks' max, mean attention-kernel ms, mean store ms)."""
+    Returns (total ms over ranks' max, median attention-kernel ms, median store ms)."""
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
@@ -367,8 +367,10 @@ def time_steps(step, steps: int, warmup: int, world: int, kernel_events=True, st
     torch.cuda.synchronize()
     barrier(world)
     total = max_over_ranks(start.elapsed_time(end), world)
-    kern = statistics.mean(a.elapsed_time(b) for a, b in evs) if evs else None
-    st = statistics.mean(a.elapsed_time(b) for a, b in sevs) if sevs else None
+    # per-launch durations: the median, since the first timed step starts on
+    # an idle GPU and its events also span the host's launch preparation
+    kern = statistics.median(a.elapsed_time(b) for a, b in evs) if evs else None
+    st = statistics.median(a.elapsed_time(b) for a, b in sevs) if sevs else None
     return total, kern, st
 
 

@@ -57,7 +57,7 @@ typedef struct CUstream_st *pkv_stream_t;  /* same type as cudaStream_t */
 enum {
     PKV_OK = 0,
     PKV_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shapes */
-    PKV_ERR_UNSUPPORTED = 2,   /* a valid request this build does not handle (e.g. head_dim) */
+    PKV_ERR_UNSUPPORTED = 2,   /* a valid request the library does not handle (e.g. head_dim) */
     PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than the *_workspace_size() */
     PKV_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed */
     PKV_ERR_DEVICE_CHECK = 5,  /* validate mode: the device flagged invalid data */

@@ -563,17 +563,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 live = wait_or_abort(&slot_full[sv], (uint32_t)(nv / kSlots) & 1u, abort_flag);
                 if (live && p.paged && !next && (j + 1) * kBN > Lk)
                     live = wait_or_abort(v_fix, 0, abort_flag);
+                // K_{j+1} too, while the tensor pipe still works through the
+                // previous tile's last S products
+                if (live && next)
+                    live = wait_or_abort(&slot_full[nk % kSlots], (uint32_t)(nk / kSlots) & 1u, abort_flag);
                 for (int t = 0; t < ntile && live; ++t) {
                     live = wait_or_abort(&p_full[t], (uint32_t)j & 1u, abort_flag);
                     if (!live) break;
                     tc_fence_after();
                     issue_PV(j, t);
-                    if (next) {
-                        if (t == 0)
-                            live = wait_or_abort(&slot_full[nk % kSlots], (uint32_t)(nk / kSlots) & 1u,
-                                                 abort_flag);
-                        if (live) issue_S(j + 1, t);
-                    }
+                    if (next) issue_S(j + 1, t);
                 }
                 if (live) {
                     umma_commit(&slot_free[sv]);                    // V_j

@@ -591,3 +591,52 @@ def test_prologue_reads_each_tokens_position_and_strided_rows():
     # q and k use their own weights
     a, b = oracle.qk_norm_rope(q, k, pos, kw, qw)
     assert not np.array_equal(a, qo)
+
+
+def _check_tables(work, nblk):
+    """Each sequence owns ceil(len / bs) distinct pool blocks, no block is
+    shared, and the rest of its row is -1."""
+    bt = work.block_tables
+    seen = []
+    for i, n in enumerate(nblk):
+        row = bt[i].tolist()
+        assert all(0 <= b < work.heads.num_blocks for b in row[:n]), i
+        assert all(b == -1 for b in row[n:]), i
+        seen += row[:n]
+    assert len(seen) == len(set(seen))
+
+
+def test_benchmark_workloads_follow_the_recipe():
+    """The seeded inputs have the shapes, ranges and table structure the
+    input recipe states, and the same seed gives the same inputs."""
+    bs = 256
+    dec = W.qwen3_decode()
+    h = dec.heads
+    assert (h.num_heads, h.num_kv_heads, h.head_dim, h.block_size, h.num_blocks) == (16, 8, 128, bs, 2048)
+    ctx = dec.context_lens
+    assert dec.batch == 64 and int(ctx.min()) >= 512 and int(ctx.max()) <= 4096
+    _check_tables(dec, [(c + bs - 1) // bs for c in ctx.tolist()])
+    again = W.qwen3_decode()
+    assert torch.equal(again.context_lens, ctx) and torch.equal(again.q, dec.q)
+
+    pre = W.varlen_prefill()
+    lens = pre.q_lens.tolist()
+    assert len(lens) == 8 and all(128 <= n <= 4096 for n in lens) and pre.total_q == 19576
+    assert torch.equal(pre.cu_seqlens_q, pre.cu_seqlens_k) and int(pre.prefix_lens.sum()) == 0
+
+    px = W.prefix_prefill()
+    assert px.num_seqs == 16
+    assert all(p % bs == 0 and 0 <= p <= 12 * bs for p in px.prefix_lens.tolist())
+    assert all(64 <= c <= 1024 for c in px.q_lens.tolist())
+    tot = (px.prefix_lens + px.q_lens).tolist()
+    assert (px.cu_seqlens_k[1:] - px.cu_seqlens_k[:-1]).tolist() == tot
+    _check_tables(px, [(t + bs - 1) // bs for t in tot])
+    pu = W.prefix_prefill(unaligned=True)
+    assert all(p % bs != 0 for p in pu.prefix_lens.tolist())
+
+    lg = W.large_decode()
+    assert (lg.heads.num_heads, lg.heads.num_kv_heads, lg.heads.num_blocks) == (32, 8, 40000)
+    c = lg.context_lens.tolist()
+    assert len(c) == 288 and all(v == 0 for v in c[256:])
+    assert all(1024 <= v <= 32768 for v in c[:256])
+    _check_tables(lg, [(v + bs - 1) // bs for v in c])

@@ -69,7 +69,9 @@ enum {
     PKV_STATUS_BAD_SLOT = 1u << 0,    /* kv_store: slot < -1 or >= num_slots        */
     PKV_STATUS_BAD_BLOCK = 1u << 1,   /* block table entry < 0 or >= num_blocks     */
     PKV_STATUS_BAD_LENGTH = 1u << 2,  /* length above its declared maximum / table   */
-    PKV_STATUS_TIMEOUT = 1u << 3      /* a bounded wait on an mbarrier expired        */
+    PKV_STATUS_TIMEOUT = 1u << 3,     /* a bounded wait on an mbarrier expired        */
+    PKV_STATUS_DUP_SLOT = 1u << 4     /* validate mode: two tokens of one call write
+                                         the same slot (a write race, L17 §5.1)     */
 };
 
 /* Message describing the last error returned on this host thread ("" if none). */
@@ -80,13 +82,25 @@ int pkv_version(void);
 
 /* Validate mode: when on, every entry point synchronises `stream` after its
  * launches and turns a non-zero device status into PKV_ERR_DEVICE_CHECK or
- * PKV_ERR_DEVICE_TIMEOUT (clearing it).  Off by default; the environment
- * variable PKV_VALIDATE=1 turns it on at load time. */
+ * PKV_ERR_DEVICE_TIMEOUT (clearing it).  The entry points that write the
+ * cache (kv_store, qk_norm_rope_store, paged_attn_decode_store) also check,
+ * in validate mode only, that no two tokens of the call write the same slot
+ * (PKV_STATUS_DUP_SLOT); the check compares every pair of slots on the device
+ * and is meant for debugging, not for the hot path.  Off by default; the
+ * environment variable PKV_VALIDATE=1 turns it on at load time. */
 void pkv_set_validate(int on);
 
 /* Synchronise `stream`, then OR together the status words of every kernel
  * family of the current device into *status; clear them when `clear` != 0. */
 int pkv_device_status(pkv_stream_t stream, uint32_t *status, int clear);
+
+/* Tuning and test control of the decode split (no counterpart in the pages):
+ * with tiles > 0 every later decode launch splits each sequence's keys into
+ * chunks of tiles * 32 keys instead of the automatic plan (tiles == 0, the
+ * default).  The chunk size changes paged_attn_decode_workspace_size(), so
+ * set it before sizing workspaces.  Process-wide; returns PKV_ERR_INVALID_ARG
+ * outside [0, 4096]. */
+int pkv_set_decode_chunk_tiles(int tiles);
 
 /* ------------------------------------------------------------------------
  * kv_build_slot_mapping -- Lesson 04, §2 (and §7, Exercise A).
@@ -138,8 +152,9 @@ int kv_build_decode_slots(const int32_t *block_tables, int64_t bt_stride,
  *               key_row_stride / value_row_stride (>= D)
  *   k_cache, v_cache  num_slots * D bf16 each
  *   slot_mapping [num_tokens] int32
- * Two tokens with the same slot in one call race (invalid input).  A slot
- * outside [-1, num_slots) is skipped and sets PKV_STATUS_BAD_SLOT.
+ * Two tokens with the same slot in one call race (invalid input; validate
+ * mode flags it with PKV_STATUS_DUP_SLOT).  A slot outside [-1, num_slots)
+ * is skipped and sets PKV_STATUS_BAD_SLOT.
  * ---------------------------------------------------------------------- */
 int kv_store(const pkv_bf16 *key, int64_t key_row_stride,
              const pkv_bf16 *value, int64_t value_row_stride,
@@ -156,9 +171,10 @@ int kv_store(const pkv_bf16 *key, int64_t key_row_stride,
  *   RMSNorm (layernorm module of "Nano-VLLM full-code notes (5)"):
  *     y = bf16( bf16( x / sqrt(mean(x^2) + rms_eps) ) * w )   (fp32 inside)
  *     with w = q_norm_weight or k_norm_weight [head_dim] bf16;
- *   RoPE (RoFormer, rotate-half pairing; the pages apply it, L17 §4, but do
- *   not print it): element e < head_dim/2 pairs with e + head_dim/2, pair i
- *   turns by a_i = positions[n] * rope_theta^(-2i/head_dim):
+ *   RoPE (the pages apply it, L17 §4, but do not print it; read as the
+ *   split-halves "rotate-half" pairing of the engine's model family, not the
+ *   adjacent pairs of RoFormer §3.2): element e < head_dim/2 pairs with
+ *   e + head_dim/2, pair i turns by a_i = positions[n] * rope_theta^(-2i/head_dim):
  *     out[i]       = y[i] cos a_i - y[i + d/2] sin a_i
  *     out[i + d/2] = y[i + d/2] cos a_i + y[i] sin a_i      (fp32, then bf16)
  * Rotated q goes to q_out; rotated k goes to k_out when k_out != NULL, and,
@@ -286,7 +302,7 @@ size_t paged_attn_decode_workspace_size(int32_t batch, int32_t num_heads,
  * Padding rows (context_lens[b] == 0) write nothing.  A block-table entry
  * outside [0, num_blocks) at the new position skips the write and sets
  * PKV_STATUS_BAD_BLOCK.  Two rows whose new positions map to the same slot
- * race (invalid input).  All other arguments, the workspace and the
+ * race (invalid input; validate mode flags it with PKV_STATUS_DUP_SLOT).  All other arguments, the workspace and the
  * supported shapes are those of paged_attn_decode.
  * ---------------------------------------------------------------------- */
 int paged_attn_decode_store(const pkv_bf16 *q, int64_t q_row_stride,
@@ -318,7 +334,10 @@ int paged_attn_decode_store(const pkv_bf16 *q, int64_t q_row_stride,
  *     a message saying so; nothing is launched.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
- *     stream capture on the device.
+ *     stream capture on the device.  The address is kept for the life of the
+ *     process: it assumes the device's primary context, in which the CUDA
+ *     runtime loaded the library, is not destroyed while the library is in
+ *     use (no cudaDeviceReset between calls).
  *   - Every call shares the one array, which keeps the last call's contents
  *     (nothing in it needs to start at zero).  Calls that can overlap on the
  *     GPU (different streams, or several host threads, without ordering

@@ -17,9 +17,13 @@
  *        FlashAttention calls, §7 Exercise A, §9 code hunt item 1.
  *   [P1] "Nano-VLLM full-code notes (5): layernorm & attention"
  *        (m.demingchina.com), the RMSNorm module (layernorm.py).
- *   [RoFormer] Su et al., "RoFormer: Enhanced Transformer with Rotary
- *        Position Embedding" (2021), the rotary position embedding that
- *        [P2] §4 applies after QK-Norm but does not print.
+ *   [P2] §4 applies a rotary position embedding after QK-Norm but does
+ *        not print it (it defers to an earlier lesson that is not among the
+ *        pages).  The reading taken is the split-halves ("rotate-half")
+ *        pairing used by the engine's model family: element e < d/2 pairs
+ *        with e + d/2.  (RoFormer, Su et al. 2021, §3.2, writes the same
+ *        rotation over adjacent pairs (x_2i, x_2i+1); that interleaved form is
+ *        a different permutation of the dimensions and is not computed here.)
  *
  * Arithmetic: bf16 inputs are widened exactly (bits << 16) to float and then
  * to double; every score, exponential, sum and output is computed in double
@@ -800,8 +804,10 @@ uint16_t orc_round_bf16(double x)
  * keeps the two roundings to bf16 where the module has them and computes
  * everything else in double.
  *
- * RoPE ([RoFormer] §3.2, "rotate-half" pairing): element e < d/2 pairs
- * with e + d/2; pair i turns by the angle pos * theta^(-2i/d):
+ * RoPE (a reading: [P2] §4 applies it without printing it; the
+ * split-halves "rotate-half" pairing of the engine's model family, not the
+ * adjacent pairs of RoFormer §3.2): element e < d/2 pairs with e + d/2;
+ * pair i turns by the angle pos * theta^(-2i/d):
  *     y[i]       = x[i] cos(a_i) - x[i + d/2] sin(a_i)
  *     y[i + d/2] = x[i + d/2] cos(a_i) + x[i] sin(a_i)
  * computed in double from the bf16 QK-Norm output and rounded to bf16 once.

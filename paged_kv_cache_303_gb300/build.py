@@ -46,20 +46,33 @@ def _stale(target: Path, deps) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -> Path:
-    BUILD.mkdir(exist_ok=True)
+    return _build_into(LIB, BUILD, [], force, verbose, jobs)
+
+
+def build_test_variant(tag: str, defines, force: bool = False) -> Path:
+    """A test-only copy of the library compiled with extra -D definitions
+    (for example a short device wait bound and the test hooks), under
+    _build/<tag>/.  The product library is never built with them."""
+    out = BUILD / tag
+    return _build_into(out / f"libpagedkv_{tag}.so", out, [f"-D{d}" for d in defines], force,
+                       False, None)
+
+
+def _build_into(lib: Path, objdir: Path, extra, force, verbose, jobs) -> Path:
+    objdir.mkdir(parents=True, exist_ok=True)
     headers = list(CSRC.glob("*.cuh")) + list(CSRC.glob("*.h")) + [ROOT / "include" / "pagedkv.h"]
     cc = nvcc()
     objs, todo = [], []
     for src in SOURCES:
         s = CSRC / src
-        o = BUILD / (s.stem + ".o")
+        o = objdir / (s.stem + ".o")
         objs.append(o)
         if force or _stale(o, [s, *headers]):
             todo.append((s, o))
 
     def compile_one(job):
         s, o = job
-        cmd = [cc, *_flags(verbose), "-c", str(s), "-o", str(o)]
+        cmd = [cc, *_flags(verbose), *extra, "-c", str(s), "-o", str(o)]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {s.name}:\n{r.stdout}\n{r.stderr}")
@@ -70,14 +83,14 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
             for log in ex.map(compile_one, todo):
                 if verbose and log:
                     sys.stderr.write(log)
-    if force or todo or _stale(LIB, objs):
-        tmp = LIB.with_suffix(f".so.tmp{os.getpid()}")
+    if force or todo or _stale(lib, objs):
+        tmp = lib.with_suffix(f".so.tmp{os.getpid()}")
         cmd = [cc, "-shared", *ARCH, "-o", str(tmp), *map(str, objs), "-cudart", "static"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

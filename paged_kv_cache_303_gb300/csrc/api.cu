@@ -18,7 +18,7 @@
 namespace {
 
 thread_local char g_err[512];
-int g_validate = -1;   // -1: not read from the environment yet
+std::atomic<int> g_validate{-1};   // -1: not read from the environment yet
 
 int fail(int code, const char *fmt, ...) {
     va_list ap;
@@ -34,11 +34,15 @@ int ok() {
 }
 
 bool validate_on() {
-    if (g_validate < 0) {
+    int v = g_validate.load(std::memory_order_relaxed);
+    if (v < 0) {
         const char *e = getenv("PKV_VALIDATE");
-        g_validate = (e && e[0] == '1') ? 1 : 0;
+        int expected = -1;
+        // an explicit pkv_set_validate() wins over the environment
+        g_validate.compare_exchange_strong(expected, (e && e[0] == '1') ? 1 : 0);
+        v = g_validate.load(std::memory_order_relaxed);
     }
-    return g_validate == 1;
+    return v == 1;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -95,16 +99,16 @@ int report(int code, const char *fmt, ...) {
 }
 
 int num_sms() {
-    static int cached[64];
+    static std::atomic<int> cached[kMaxDevices];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (cached[dev] <= 0) {
-        int n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = 148;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 int encode_rows_heads_map(CUtensorMap *map, const void *base, int64_t rows, int32_t heads,
@@ -135,7 +139,14 @@ const char *pkv_last_error(void) { return g_err; }
 
 int pkv_version(void) { return 1; }
 
-void pkv_set_validate(int on) { g_validate = on ? 1 : 0; }
+void pkv_set_validate(int on) { g_validate.store(on ? 1 : 0, std::memory_order_relaxed); }
+
+int pkv_set_decode_chunk_tiles(int tiles) {
+    if (tiles < 0 || tiles > 4096)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_set_decode_chunk_tiles: tiles must be in [0, 4096]");
+    pkv::g_decode_chunk_tiles.store(tiles, std::memory_order_relaxed);
+    return ok();
+}
 
 int pkv_device_status(pkv_stream_t stream, uint32_t *status, int clear) {
     if (!status) return fail(PKV_ERR_INVALID_ARG, "pkv_device_status: status is NULL");
@@ -204,6 +215,8 @@ int kv_store(const pkv_bf16 *key, int64_t key_row_stride, const pkv_bf16 *value,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = pkv::launch_kv_store(key, key_row_stride, value, value_row_stride, k_cache,
                                          v_cache, slot_mapping, num_tokens, D, num_slots, s);
+    if (e == cudaSuccess && validate_on())
+        e = pkv::launch_check_duplicate_slots(slot_mapping, nullptr, 0, 0, nullptr, 1, 0, num_tokens, s);
     if (e != cudaSuccess) return cuda_fail(e, "kv_store");
     return post_launch(s, "kv_store");
 }
@@ -268,6 +281,8 @@ int qk_norm_rope_store(const pkv_bf16 *q, int64_t q_row_stride, const pkv_bf16 *
     a.head_dim = head_dim;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = pkv::launch_qk_norm_rope_store(a, s);
+    if (e == cudaSuccess && validate_on())
+        e = pkv::launch_check_duplicate_slots(slot_mapping, nullptr, 0, 0, nullptr, 1, 0, num_tokens, s);
     if (e != cudaSuccess) return cuda_fail(e, what);
     return post_launch(s, what);
 }
@@ -371,6 +386,12 @@ static int decode_entry(const char *what, const pkv_bf16 *q, int64_t q_row_strid
     const char *err = "";
     int rc = pkv::launch_decode(a, s, &err);
     if (rc) return fail(rc, "%s: %s", what, err);
+    if (key && validate_on()) {
+        cudaError_t e = pkv::launch_check_duplicate_slots(nullptr, block_tables, bt_stride,
+                                                          max_blocks_per_seq, context_lens,
+                                                          block_size, num_blocks, batch, s);
+        if (e != cudaSuccess) return cuda_fail(e, what);
+    }
     return post_launch(s, what);
 }
 
@@ -496,3 +517,11 @@ int paged_attn_prefill(const pkv_bf16 *q, int64_t q_row_stride, const pkv_bf16 *
 }
 
 }  // extern "C"
+
+#if PKV_TEST_HOOKS
+// Only in the test-only build (never in libpagedkv.so): see decode.cu.
+namespace pkv {
+int test_withhold_decode_ready(int on);
+}
+extern "C" int pkv_test_withhold_decode_ready(int on) { return pkv::test_withhold_decode_ready(on); }
+#endif

@@ -100,8 +100,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 
 // Upper bound of a single wait: about 2^31 cycles (roughly a second at the
 // SM clock).  Each try_wait suspends the thread in hardware for up to
-// kSuspendNs, so the loop runs at most a few thousand times.
-constexpr long long kWaitCycles = 1ll << 31;
+// kSuspendNs, so the loop runs at most a few thousand times.  A test-only
+// build of the library lowers the bound (PKV_WAIT_CYCLES) so that a test can
+// let a wait run out quickly.
+#ifndef PKV_WAIT_CYCLES
+#define PKV_WAIT_CYCLES (1ll << 31)
+#endif
+constexpr long long kWaitCycles = PKV_WAIT_CYCLES;
 constexpr uint32_t kSuspendNs = 100000;
 
 // Bounded wait on an mbarrier phase.  Returns false when the bound expired;

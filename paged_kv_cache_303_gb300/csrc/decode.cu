@@ -66,6 +66,17 @@ namespace pkv {
 
 static __device__ unsigned int g_decode_status;
 
+#if PKV_TEST_HOOKS
+// Test-only build: while set, every CTA's producer withholds its arrival on
+// the first item's ready barrier, so the consumers' bounded wait runs out
+// (no bulk copy is ever pending on that barrier).
+static __device__ int g_test_withhold_ready;
+
+int test_withhold_decode_ready(int on) {
+    return cudaMemcpyToSymbol(g_test_withhold_ready, &on, sizeof on) == cudaSuccess ? 0 : -1;
+}
+#endif
+
 cudaError_t decode_status(cudaStream_t stream, uint32_t *host, bool clear) {
     unsigned int v = 0;
     cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_decode_status, sizeof v, 0,
@@ -97,11 +108,26 @@ constexpr int kConsumers = PKV_DEC_CONSUMERS;    // consumer warps per CTA
 constexpr int kThreads = (kConsumers + 1) * 32;  // + one TMA producer warp
 constexpr int kTile = 32;                        // tokens per pipeline stage (one per lane)
 constexpr int kStages = PKV_DEC_STAGES;
-// Consumer warp w takes tiles w, w + kConsumers, ... of the ring and waits on
-// the stage's full barrier by phase parity; with more warps than stages two
-// warps would wait on one stage for phases two apart, and the later one's
-// parity check would pass before its tile has landed.
-static_assert(kConsumers <= kStages, "one ring stage per consumer warp at least");
+// Ring protocol.  Tile gt of the ring (counted across items) lives in stage
+// gt % kStages and is that stage's phase K = gt / kStages.  A parity wait
+// for phase K also passes while phase K-1 is still open (its parity is the
+// one before), so a consumer may wait on full[stage] for tile gt only once
+// phase K-1 -- tile gt - kStages -- has completed.  That tile may belong to
+// the other consumer warp and TMA completions are unordered, so nothing in
+// the consumer's own history implies it.  The consumer therefore first waits
+// on empty[stage] for the release of tile gt - kStages: its consumer waited
+// for that tile's phase before releasing it, so after this wait phase K-1 of
+// full[stage] is complete, and phase K+1 cannot complete before this warp
+// releases tile gt, which makes the parity wait for K exact.  The empty wait
+// is itself exact when phase K-2 of empty[stage] (the release of tile
+// gt - 2 kStages) has completed: that tile is either in an earlier item (all
+// of whose tiles are released before the consumers' merge barrier) or this
+// warp's own tile of the current item, which holds when kConsumers divides
+// 2 kStages (tiles of an item go round-robin to the warps).  The producer
+// needs the same release before it loads tile gt, so the extra wait costs a
+// shared-memory poll, not time.
+static_assert((2 * kStages) % kConsumers == 0,
+              "tile gt - 2*kStages must be the waiting warp's own tile");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -335,6 +361,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             __syncwarp();
             if (lane == 0) {
                 items[e] = it;
+#if PKV_TEST_HOOKS
+                if (!(seq == 0 && g_test_withhold_ready))
+#endif
                 mbar_arrive(&ready[e]);                 // releases q and the record
                 // the item's tiles, tile i -> ring position g
                 const int32_t *bt_row = p.bt + (int64_t)it.b * p.bt_stride;
@@ -426,6 +455,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         for (int i = warp; i < it.ntiles; i += kConsumers) {
             const int gt = g0 + i;
             const int stage = gt % kStages;
+            // the previous tile of this stage has been released (so it had
+            // landed) before this tile's phase is awaited; see kStages above
+            if (gt >= kStages &&
+                !wait_or_abort(&empty[stage], (uint32_t)((gt / kStages) - 1) & 1u, abort_flag)) {
+                live = false;
+                break;
+            }
             if (!wait_or_abort(&full[stage], (uint32_t)(gt / kStages) & 1u, abort_flag)) {
                 live = false;
                 break;
@@ -659,23 +695,24 @@ int launch_split(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParam
                  int num_kv_heads, cudaStream_t stream, const char **err) {
     auto kern = decode_split_kernel<HD, G, SW>;
     const size_t smem = 1024 /*alignment slack*/ + Layout<HD, G>::kBytes;
-    static bool configured[64];                        // per device
-    static int resident[64];                           // CTAs of this kernel per SM
+    static PerDeviceOnce once;
+    static int resident[kMaxDevices];                  // CTAs of this kernel per SM
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = once.run(dev, [&]() -> cudaError_t {
+            cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            int nb = 0;
+            if (r == cudaSuccess)
+                r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, smem);
+            if (r == cudaSuccess) resident[dev] = nb > 0 ? nb : 1;
+            return r;
+        });
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
-    if (!configured[dev & 63]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
-        int nb = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, smem);
-        if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
-        resident[dev & 63] = nb > 0 ? nb : 1;
-        configured[dev & 63] = true;
-    }
     // one resident wave; the CTAs claim the items
     const int64_t items = (int64_t)batch * num_kv_heads * p.max_splits;
-    const int64_t wave = (int64_t)num_sms() * resident[dev & 63];
+    const int64_t wave = (int64_t)num_sms() * resident[dev];
     const dim3 grid((unsigned)(items < wave ? items : wave));
     kern<<<grid, kThreads, smem, stream>>>(km, vm, p);
     e = cudaGetLastError();
@@ -697,6 +734,8 @@ int dispatch_group(int G, const CUtensorMap &km, const CUtensorMap &vm, const De
 
 }  // namespace
 
+std::atomic<int> g_decode_chunk_tiles{0};
+
 void decode_plan(int32_t batch, int32_t num_kv_heads, int32_t head_dim, int32_t max_context_len,
                  int32_t *chunk, int32_t *max_splits) {
     (void)head_dim;
@@ -707,10 +746,8 @@ void decode_plan(int32_t batch, int32_t num_kv_heads, int32_t head_dim, int32_t 
     int64_t per = (keys + target * kTile - 1) / (target * kTile);
     if (per < 8) per = 8;
     if (per > 64) per = 64;
-    if (const char *env = getenv("PKV_DECODE_CHUNK_TILES")) {
-        const int v = atoi(env);
-        if (v >= 1 && v <= 4096) per = v;
-    }
+    const int forced = g_decode_chunk_tiles.load(std::memory_order_relaxed);
+    if (forced > 0) per = forced;
     *chunk = (int32_t)(per * kTile);
     *max_splits = max_context_len <= 0 ? 1 : (int32_t)((max_context_len + *chunk - 1) / *chunk);
 }
@@ -827,7 +864,9 @@ static __device__ __align__(256) unsigned char g_decode_static_scratch[kStaticSc
 
 // Device address of the array, looked up once per device with that device
 // current (in host code the array's name is only a host-side stand-in, never
-// a device address).
+// a device address).  The address stays valid while the device's primary
+// context lives; a cudaDeviceReset would make the kept address stale, so the
+// entry point's documentation rules that out.
 void *static_scratch_address(const char **err) {
     static std::mutex mu;
     static void *addr[64] = {};

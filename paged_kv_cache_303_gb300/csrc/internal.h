@@ -7,9 +7,37 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/pagedkv.h"
 
 namespace pkv {
+
+constexpr int kMaxDevices = 64;
+
+// One-time set-up per device (kernel attributes, occupancy queries) that is
+// safe when several host threads make their first call on a device at the
+// same time: the first caller runs `fn` under a lock, the others wait for it;
+// a failed set-up is retried by the next call.  Values `fn` writes are
+// visible to every caller that sees run() return cudaSuccess.
+class PerDeviceOnce {
+  public:
+    template <class F>
+    cudaError_t run(int dev, F &&fn) {
+        if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+        const cudaError_t e = fn();
+        if (e == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+        return e;
+    }
+
+  private:
+    std::mutex mu_;
+    std::atomic<bool> done_[kMaxDevices] = {};
+};
 
 // Each kernel translation unit keeps its own sticky device status word
 // (PKV_STATUS_* bits).  These read (and optionally clear) it on `stream`.
@@ -28,6 +56,14 @@ cudaError_t launch_decode_slots(const int32_t *bt, int64_t bt_stride, int32_t ma
 cudaError_t launch_kv_store(const uint16_t *key, int64_t key_rs, const uint16_t *value,
                             int64_t value_rs, uint16_t *kc, uint16_t *vc, const int32_t *slots,
                             int32_t n, int64_t D, int64_t num_slots, cudaStream_t stream);
+
+// Validate mode: flag PKV_STATUS_DUP_SLOT when two of the n tokens write the
+// same slot.  The slots are slots[i] when `slots` is given, else the decode
+// slot of row i (position ctx[i]-1 through the block table; none for ctx 0).
+cudaError_t launch_check_duplicate_slots(const int32_t *slots, const int32_t *bt, int64_t bt_stride,
+                                         int32_t max_blocks, const int32_t *ctx,
+                                         int32_t block_size, int64_t num_blocks, int32_t n,
+                                         cudaStream_t stream);
 
 struct PrologueArgs {
     const uint16_t *q;
@@ -73,6 +109,8 @@ struct DecodeArgs {
     const uint16_t *new_k, *new_v;
     int64_t new_k_rs, new_v_rs;
 };
+// keys per split chunk forced by pkv_set_decode_chunk_tiles (0: automatic)
+extern std::atomic<int> g_decode_chunk_tiles;
 // chunk of keys per split and number of splits for a decode launch
 void decode_plan(int32_t batch, int32_t num_kv_heads, int32_t head_dim, int32_t max_context_len,
                  int32_t *chunk, int32_t *max_splits);

@@ -187,8 +187,10 @@ __global__ void __launch_bounds__(kStoreWarps * 32) kv_store_scalar_kernel(
 //
 // RMSNorm as the layernorm module of "Nano-VLLM full-code notes (5)" does
 // it: x / sqrt(mean(x^2) + eps) in fp32, rounded to bf16, then the bf16
-// product with the weight (rounded to bf16).  RoPE (RoFormer, rotate-half
-// pairing): element e < d/2 pairs with e + d/2 and pair i turns by
+// product with the weight (rounded to bf16).  RoPE (applied by L17 §4 but
+// not printed there; read as the split-halves "rotate-half" pairing of the
+// engine's model family, not RoFormer's adjacent pairs): element e < d/2
+// pairs with e + d/2 and pair i turns by
 // pos * theta^(-2i/d); the rotation is computed in fp32 from the bf16 norm
 // output and rounded to bf16 once.
 //
@@ -530,23 +532,81 @@ cudaError_t launch_qk_norm_rope_store(const PrologueArgs &a, cudaStream_t stream
     const int64_t wave = (int64_t)num_sms() * PKV_PRO_MIN_CTAS;
     const dim3 grid((unsigned)(need < wave ? need : wave));
     const int smem = kProWarps * (a.head_dim == 128 ? ProStage<128>::kWarpBytes : ProStage<64>::kWarpBytes);
-    static bool configured[64];                 // per device
+    static PerDeviceOnce once;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = once.run(dev, []() {
+            cudaError_t r = cudaFuncSetAttribute(qk_norm_rope_store_kernel<128>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kProWarps * ProStage<128>::kWarpBytes);
+            if (r == cudaSuccess)
+                r = cudaFuncSetAttribute(qk_norm_rope_store_kernel<64>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kProWarps * ProStage<64>::kWarpBytes);
+            return r;
+        });
     if (e != cudaSuccess) return e;
-    if (!configured[dev & 63]) {
-        e = cudaFuncSetAttribute(qk_norm_rope_store_kernel<128>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kProWarps * ProStage<128>::kWarpBytes);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(qk_norm_rope_store_kernel<64>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kProWarps * ProStage<64>::kWarpBytes);
-        if (e != cudaSuccess) return e;
-        configured[dev & 63] = true;
-    }
     if (a.head_dim == 128)
         qk_norm_rope_store_kernel<128><<<grid, kProWarps * 32, smem, stream>>>(p);
     else
         qk_norm_rope_store_kernel<64><<<grid, kProWarps * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Duplicate-slot check (validate mode only): every pair (i, j), i < j, of the
+// call's written slots is compared; a CTA holds 256 tokens' slots in
+// registers and streams the later tokens' slots through shared memory.
+// ---------------------------------------------------------------------------
+struct SlotSource {
+    const int32_t *slots;       // given slots, or null: derive decode slots
+    const int32_t *bt;
+    int64_t bt_stride;
+    int32_t max_blocks;
+    const int32_t *ctx;
+    int32_t block_size;
+    int64_t num_blocks;
+};
+
+// the slot token i writes, -1 when it writes nothing
+__device__ __forceinline__ int32_t written_slot(const SlotSource &s, int32_t i) {
+    if (s.slots) return s.slots[i];
+    const int64_t c = s.ctx[i];
+    if (c <= 0) return -1;
+    const int64_t p = c - 1;
+    const int64_t lb = p / s.block_size;
+    const int32_t blk = lb < s.max_blocks ? s.bt[(int64_t)i * s.bt_stride + lb] : -1;
+    if (blk < 0 || blk >= s.num_blocks) return -1;
+    return (int32_t)((int64_t)blk * s.block_size + p % s.block_size);
+}
+
+constexpr int kDupThreads = 256;
+
+__global__ void __launch_bounds__(kDupThreads) duplicate_slots_kernel(SlotSource src, int32_t n) {
+    __shared__ int32_t later[kDupThreads];
+    const int32_t i = blockIdx.x * kDupThreads + threadIdx.x;
+    const int32_t mine = i < n ? written_slot(src, i) : -1;
+    bool dup = false;
+    for (int32_t j0 = blockIdx.x * kDupThreads; j0 < n; j0 += kDupThreads) {
+        __syncthreads();
+        later[threadIdx.x] = j0 + (int32_t)threadIdx.x < n ? written_slot(src, j0 + threadIdx.x) : -1;
+        __syncthreads();
+        if (mine >= 0) {
+            for (int t = 0; t < kDupThreads; ++t)
+                dup |= j0 + t > i && later[t] == mine;
+        }
+    }
+    if (dup) flag(PKV_STATUS_DUP_SLOT);
+}
+
+cudaError_t launch_check_duplicate_slots(const int32_t *slots, const int32_t *bt, int64_t bt_stride,
+                                         int32_t max_blocks, const int32_t *ctx,
+                                         int32_t block_size, int64_t num_blocks, int32_t n,
+                                         cudaStream_t stream) {
+    if (n <= 1) return cudaSuccess;
+    SlotSource s{slots, bt, bt_stride, max_blocks, ctx, block_size, num_blocks};
+    duplicate_slots_kernel<<<(n + kDupThreads - 1) / kDupThreads, kDupThreads, 0, stream>>>(s, n);
     return cudaGetLastError();
 }
 

@@ -722,15 +722,14 @@ int launch_hd(const PrefillArgs &a, const PrefillParams &pp, int2 *work, int32_t
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
     const int smem = L::kBytes + 1024;
     auto kern = prefill_kernel<HD>;
-    static bool configured[64];                        // per device
+    static PerDeviceOnce once;
     int dev = 0;
     e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = once.run(dev, [&]() {
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        });
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
-    if (!configured[dev & 63]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
-        configured[dev & 63] = true;
-    }
     const int G = a.num_heads / a.num_kv_heads;
     const int ntile = G >= 2 ? 2 : 1;
     cudaLaunchConfig_t cfg = {};

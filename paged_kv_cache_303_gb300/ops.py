@@ -23,6 +23,7 @@ PKV_STATUS_BAD_SLOT = 1
 PKV_STATUS_BAD_BLOCK = 2
 PKV_STATUS_BAD_LENGTH = 4
 PKV_STATUS_TIMEOUT = 8
+PKV_STATUS_DUP_SLOT = 16
 
 _ERRNAMES = {1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_WORKSPACE",
              4: "PKV_ERR_CUDA", 5: "PKV_ERR_DEVICE_CHECK", 6: "PKV_ERR_DEVICE_TIMEOUT"}
@@ -42,6 +43,7 @@ SIGNATURES = {
     "pkv_version": ([], _INT),
     "pkv_set_validate": ([_INT], None),
     "pkv_device_status": ([_P, _P, _INT], _INT),
+    "pkv_set_decode_chunk_tiles": ([_INT], _INT),
     "kv_build_slot_mapping": ([_P, _I64, _I32, _P, _P, _I32, _I32, _P, _I32, _P], _INT),
     "kv_build_decode_slots": ([_P, _I64, _I32, _P, _I32, _I32, _P, _P], _INT),
     "kv_store": ([_P, _I64, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _I64, _P], _INT),
@@ -131,6 +133,11 @@ def _ptr(t: Optional[torch.Tensor]):
 
 def set_validate(on: bool):
     lib().pkv_set_validate(1 if on else 0)
+
+
+def set_decode_chunk_tiles(tiles: int):
+    """Force decode chunks of tiles*32 keys (0 restores the automatic plan)."""
+    _check(lib().pkv_set_decode_chunk_tiles(int(tiles)))
 
 
 def device_status(clear: bool = True, device=None) -> int:

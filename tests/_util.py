@@ -1,4 +1,5 @@
 """Small helpers shared by the tests (no method arithmetic)."""
+import contextlib
 import json
 import os
 
@@ -34,3 +35,15 @@ def bf16_bits_of(values) -> np.ndarray:
     b = t.to(torch.bfloat16)
     assert torch.equal(b.to(torch.float32), t), "value not exact in bf16"
     return b.view(torch.int16).numpy().view(np.uint16)
+
+
+@contextlib.contextmanager
+def decode_chunk_tiles(tiles):
+    """Force decode chunks of tiles*32 keys inside the block (None or 0: the
+    library's automatic plan), restoring the automatic plan afterwards."""
+    from paged_kv_cache_303_gb300 import ops
+    ops.set_decode_chunk_tiles(int(tiles or 0))
+    try:
+        yield
+    finally:
+        ops.set_decode_chunk_tiles(0)

@@ -142,3 +142,18 @@ def test_fused_entry_points_validate_before_launch(lib):
     # zero tokens is a valid no-op
     assert lib.qk_norm_rope_store(None, 0, None, 0, None, 0, None, None, None, 1e-6, 1e6, None, 0,
                                   None, 0, None, None, None, 0, 4, 1, 128, 0, None) == 0
+
+
+def test_decode_chunk_tiles_setter_sizes_the_workspace(lib):
+    auto = lib.paged_attn_decode_workspace_size(4, 16, 8, 128, 4096)
+    try:
+        assert lib.pkv_set_decode_chunk_tiles(1) == 0
+        # 32-key chunks: 128 splits of a 4096-key context, each with a
+        # head_dim row and an (m, l) pair per (row, head)
+        forced = lib.paged_attn_decode_workspace_size(4, 16, 8, 128, 4096)
+        assert forced >= 256 + 4 * 16 * 128 * (128 + 2) * 4
+        assert lib.pkv_set_decode_chunk_tiles(-1) == 1
+        assert lib.pkv_set_decode_chunk_tiles(4097) == 1
+    finally:
+        assert lib.pkv_set_decode_chunk_tiles(0) == 0
+    assert lib.paged_attn_decode_workspace_size(4, 16, 8, 128, 4096) == auto < forced

@@ -40,11 +40,12 @@ def _fused(work, gk, gv, max_ctx):
 
 
 @pytest.mark.parametrize("shape", DECODE_SHAPES, ids=lambda s: f"{s[0]}q{s[1]}kv{s[2]}d_bs{s[3]}")
-@pytest.mark.parametrize("chunk_tiles", [None, "1"])
-def test_decode_store_vs_oracle_and_unfused(shape, chunk_tiles, monkeypatch):
+@pytest.mark.parametrize("chunk_tiles", [None, 1])
+def test_decode_store_vs_oracle_and_unfused(shape, chunk_tiles, request):
     hq, hkv, d, bs, ctx = shape
     if chunk_tiles:
-        monkeypatch.setenv("PKV_DECODE_CHUNK_TILES", chunk_tiles)
+        ops.set_decode_chunk_tiles(chunk_tiles)
+        request.addfinalizer(lambda: ops.set_decode_chunk_tiles(0))
     need = sum((c + bs - 1) // bs for c in ctx) + 3
     heads = W.Heads(hq, hkv, d, bs, need)
     work = W.decode_work(heads, ctx, seed=700 + hq + d + bs)
@@ -189,11 +190,12 @@ def test_decode_store_step_replayed_as_cuda_graph():
 
 
 @pytest.mark.parametrize("fused", [False, True])
-def test_chunk_merge_with_dirty_workspace_twice(fused, monkeypatch):
+def test_chunk_merge_with_dirty_workspace_twice(fused, request):
     """Chunks of 32 keys (up to 64 per sequence), a workspace full of 0xFF
     bytes and two calls in a row on it: the chunk counters and partials must
     not depend on what the workspace held before."""
-    monkeypatch.setenv("PKV_DECODE_CHUNK_TILES", "1")
+    ops.set_decode_chunk_tiles(1)
+    request.addfinalizer(lambda: ops.set_decode_chunk_tiles(0))
     heads = W.Heads(16, 8, 128, 64, 128)
     ctx = [1, 31, 32, 33, 64, 65, 1000, 2047, 2048, 0, 7]
     work = W.decode_work(heads, ctx, seed=880)

@@ -16,7 +16,7 @@ import torch
 import oracle
 from paged_kv_cache_303_gb300 import ops
 from paged_kv_cache_303_gb300 import workloads as W
-from _util import bits, bf16_bits_of, f64, from_bits, golden
+from _util import bits, bf16_bits_of, decode_chunk_tiles, f64, from_bits, golden
 
 pytestmark = pytest.mark.gpu
 
@@ -217,14 +217,13 @@ DECODE_SHAPES = [
 
 
 @pytest.mark.parametrize("shape", DECODE_SHAPES, ids=lambda s: f"{s[0]}q{s[1]}kv{s[2]}d_bs{s[3]}")
-@pytest.mark.parametrize("chunk_tiles", [None, "1", "3"])
-def test_decode_vs_oracle(shape, chunk_tiles, monkeypatch):
+@pytest.mark.parametrize("chunk_tiles", [None, 1, 3])
+def test_decode_vs_oracle(shape, chunk_tiles):
     hq, hkv, d, bs, ctx = shape
-    if chunk_tiles:
-        monkeypatch.setenv("PKV_DECODE_CHUNK_TILES", chunk_tiles)
     need = sum((c + bs - 1) // bs for c in ctx) + 3
     heads = W.Heads(hq, hkv, d, bs, need)
-    _decode_case(heads, ctx, seed=300 + hq + d + bs)
+    with decode_chunk_tiles(chunk_tiles):
+        _decode_case(heads, ctx, seed=300 + hq + d + bs)
 
 
 @pytest.mark.parametrize("bs", [1, 2, 8, 128])
@@ -291,7 +290,7 @@ def test_decode_qwen3_full_size():
 
 
 def _compact_blocks(block_tables, rows, lens):
-    """For sampled rows, the physical blocks they read and a table remapped to
+    """For the given rows, the physical blocks they read and a table remapped to
     a compact cache holding only those blocks."""
     bs_rows = block_tables[rows]
     used = sorted({int(b) for r, n in zip(bs_rows.tolist(), lens) for b in r[:n] if b >= 0})
@@ -303,15 +302,15 @@ def _compact_blocks(block_tables, rows, lens):
     return used, table
 
 
-def test_decode_large_padded_sampled():
+def test_decode_large_padded_full_size():
     """Batch 256 + 32 padding rows, GQA group 4, lognormal contexts up to 32k,
-    40000-block pool (40 GiB of K/V on the device): checked on sampled rows."""
+    40000-block pool (40 GiB of K/V on the device), in the launch the
+    benchmark times: every row and every head against the oracle, on a
+    compacted copy of all the blocks the live rows read."""
     work = W.large_decode()
     h = work.heads
     lens = work.context_lens.numpy()
-    rng = np.random.default_rng(5)
-    rows = sorted(set([int(np.argmax(lens)), int(np.argmin(lens[:256])), 256, 287] +
-                      rng.choice(256, 12, replace=False).tolist()))
+    rows = list(range(work.batch))
     nblk = [int((lens[r] + h.block_size - 1) // h.block_size) for r in rows]
     used, table = _compact_blocks(work.block_tables.numpy(), rows, nblk)
     shape = (h.num_blocks, h.block_size, h.num_kv_heads, h.head_dim)
@@ -329,18 +328,17 @@ def test_decode_large_padded_sampled():
     out, lse = ops.paged_attn_decode(dev(work.q), gk, gv, bt, ctx, work.max_context_len, h.scale,
                                      return_lse=True)
     torch.cuda.synchronize()
-    sub_ctx = lens[rows]
-    slots = oracle.decode_slots(table, sub_ctx, h.block_size)
-    oracle.kv_store(bits(work.k[rows]), bits(work.v[rows]), kref, vref, slots)
-    ref, ref_lse = oracle.decode(bits(work.q[rows]), kref, vref, table, sub_ctx, h.scale)
-    assert_close(out[rows], ref, "large decode (sampled rows)")
-    got = lse[rows].cpu().double().numpy()
+    del gk, gv, idx
+    torch.cuda.empty_cache()
+    slots = oracle.decode_slots(table, lens, h.block_size)
+    oracle.kv_store(bits(work.k), bits(work.v), kref, vref, slots)
+    ref, ref_lse = oracle.decode(bits(work.q), kref, vref, table, lens, h.scale)
+    assert_close(out, ref, "large decode (all rows)")
+    got = lse.cpu().double().numpy()
     fin = np.isfinite(ref_lse)
     assert np.array_equal(np.isfinite(got), fin)
     assert np.allclose(got[fin], ref_lse[fin], atol=2e-3, rtol=1e-4)
     assert out[256:].eq(0).all()
-    del gk, gv
-    torch.cuda.empty_cache()
 
 
 # ---------------------------------------------------------------------------
@@ -458,31 +456,33 @@ def test_prefill_paged_group4_d64():
     _prefill_paged(heads, [90, 200], [40, 0], seed=780)
 
 
-def test_prefill_varlen_full_size_sampled():
-    """8 prompts of U[128, 4096] tokens (about 16k), packed: sampled rows."""
+def _check_lse(lse, ref_lse, what):
+    got = lse.cpu().double().numpy()
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(got), fin), what
+    assert np.allclose(got[fin], ref_lse[fin], atol=2e-3, rtol=1e-4), what
+
+
+def test_prefill_varlen_full_size():
+    """8 prompts of U[128, 4096] tokens (about 19.6k), packed, as the
+    benchmark runs them: every output element and every lse against the
+    oracle."""
     work = W.varlen_prefill()
     h = work.heads
-    out = ops.paged_attn_prefill(dev(work.q), dev(work.k), dev(work.v), dev(work.cu_seqlens_q),
-                                 dev(work.cu_seqlens_k), work.max_seqlen_q, work.max_seqlen_k,
-                                 h.scale)
+    out, lse = ops.paged_attn_prefill(dev(work.q), dev(work.k), dev(work.v),
+                                      dev(work.cu_seqlens_q), dev(work.cu_seqlens_k),
+                                      work.max_seqlen_q, work.max_seqlen_k, h.scale,
+                                      return_lse=True)
     torch.cuda.synchronize()
-    cu = work.cu_seqlens_q.tolist()
-    rng = np.random.default_rng(11)
-    rows = set(rng.choice(work.total_q, 48, replace=False).tolist())
-    for i in range(work.num_seqs):
-        rows |= {cu[i], cu[i + 1] - 1, min(cu[i] + 128, cu[i + 1] - 1)}
-    rows = sorted(rows)
-    ref, _ = oracle.prefill_rows(bits(work.q), bits(work.k), bits(work.v), work.cu_seqlens_q,
-                                 work.cu_seqlens_k, h.scale, rows)
-    assert_close(out[rows], ref, "varlen prefill (sampled rows)")
+    ref, ref_lse = oracle.prefill(bits(work.q), bits(work.k), bits(work.v), work.cu_seqlens_q,
+                                  work.cu_seqlens_k, h.scale)
+    assert_close(out, ref, "varlen prefill (all rows)")
+    _check_lse(lse, ref_lse, "varlen prefill lse")
 
 
-def test_prefill_prefix_full_size_sampled():
-    """16 sequences, cached prefix of U{0..12} blocks of 256 plus a chunk of
-    U[64, 1024] tokens read through block_tables: sampled rows."""
-    work = W.prefix_prefill()
+def _prefix_full_size(work, seed):
     h = work.heads
-    kc, vc = W.history_cache(h, 801)
+    kc, vc = W.history_cache(h, seed)
     kref, vref = bits(kc).copy(), bits(vc).copy()
     slots = oracle.slot_mapping(work.block_tables, work.prefix_lens, work.cu_seqlens_q,
                                 h.block_size)
@@ -491,47 +491,34 @@ def test_prefill_prefix_full_size_sampled():
     bt = dev(work.block_tables)
     gs = ops.kv_build_slot_mapping(bt, dev(work.prefix_lens), dev(work.cu_seqlens_q), h.block_size)
     ops.kv_store(dev(work.k), dev(work.v), gk, gv, gs)
-    out = ops.paged_attn_prefill(dev(work.q), None, None, dev(work.cu_seqlens_q),
-                                 dev(work.cu_seqlens_k), work.max_seqlen_q, work.max_seqlen_k,
-                                 h.scale, k_cache=gk, v_cache=gv, block_tables=bt)
+    out, lse = ops.paged_attn_prefill(dev(work.q), None, None, dev(work.cu_seqlens_q),
+                                      dev(work.cu_seqlens_k), work.max_seqlen_q, work.max_seqlen_k,
+                                      h.scale, k_cache=gk, v_cache=gv, block_tables=bt,
+                                      return_lse=True)
     torch.cuda.synchronize()
-    assert np.array_equal(gs.cpu().numpy(), slots)
-    rng = np.random.default_rng(12)
-    cu = work.cu_seqlens_q.tolist()
-    rows = set(rng.choice(work.total_q, 40, replace=False).tolist())
-    for i in range(work.num_seqs):
-        rows |= {cu[i], cu[i + 1] - 1}
-    rows = sorted(rows)
-    ref, _ = oracle.prefill_rows(bits(work.q), None, None, work.cu_seqlens_q, work.cu_seqlens_k,
-                                 h.scale, rows, k_cache=kref, v_cache=vref,
-                                 block_tables=work.block_tables)
-    assert_close(out[rows], ref, "prefix prefill (sampled rows)")
-
-
-def test_prefill_unaligned_prefix_full_size_sampled():
-    work = W.prefix_prefill(unaligned=True)
-    h = work.heads
-    kc, vc = W.history_cache(h, 811)
-    kref, vref = bits(kc).copy(), bits(vc).copy()
-    slots = oracle.slot_mapping(work.block_tables, work.prefix_lens, work.cu_seqlens_q,
-                                h.block_size)
-    oracle.kv_store(bits(work.k), bits(work.v), kref, vref, slots)
-    gk, gv = dev(kc), dev(vc)
-    bt = dev(work.block_tables)
-    gs = ops.kv_build_slot_mapping(bt, dev(work.prefix_lens), dev(work.cu_seqlens_q), h.block_size)
-    ops.kv_store(dev(work.k), dev(work.v), gk, gv, gs)
     assert np.array_equal(gs.cpu().numpy(), slots)
     assert np.array_equal(bits(gk), kref) and np.array_equal(bits(gv), vref)
-    out = ops.paged_attn_prefill(dev(work.q), None, None, dev(work.cu_seqlens_q),
-                                 dev(work.cu_seqlens_k), work.max_seqlen_q, work.max_seqlen_k,
-                                 h.scale, k_cache=gk, v_cache=gv, block_tables=bt)
-    torch.cuda.synchronize()
-    cu = work.cu_seqlens_q.tolist()
-    rows = sorted({cu[i] for i in range(work.num_seqs)} | {cu[i + 1] - 1 for i in range(work.num_seqs)})
-    ref, _ = oracle.prefill_rows(bits(work.q), None, None, work.cu_seqlens_q, work.cu_seqlens_k,
-                                 h.scale, rows, k_cache=kref, v_cache=vref,
-                                 block_tables=work.block_tables)
-    assert_close(out[rows], ref, "unaligned prefix prefill (sampled rows)")
+    ref, ref_lse = oracle.prefill(bits(work.q), None, None, work.cu_seqlens_q, work.cu_seqlens_k,
+                                  h.scale, k_cache=kref, v_cache=vref,
+                                  block_tables=work.block_tables)
+    return out, lse, ref, ref_lse
+
+
+def test_prefill_prefix_full_size():
+    """16 sequences, cached prefix of U{0..12} blocks of 256 plus a chunk of
+    U[64, 1024] tokens read through block_tables, as the benchmark runs
+    them: every output element and every lse against the oracle."""
+    out, lse, ref, ref_lse = _prefix_full_size(W.prefix_prefill(), 801)
+    assert_close(out, ref, "prefix prefill (all rows)")
+    _check_lse(lse, ref_lse, "prefix prefill lse")
+
+
+def test_prefill_unaligned_prefix_full_size():
+    """The same with prefixes that end mid-block (256 p + U[1, 255]), so every
+    chunk starts mid-block: every output element and every lse."""
+    out, lse, ref, ref_lse = _prefix_full_size(W.prefix_prefill(unaligned=True), 811)
+    assert_close(out, ref, "unaligned prefix prefill (all rows)")
+    _check_lse(lse, ref_lse, "unaligned prefix prefill lse")
 
 
 def test_decode_equals_last_prefill_row_on_gpu():
@@ -562,6 +549,45 @@ def test_validate_mode_reports_bad_table():
         assert e.value.code == 5
     finally:
         ops.set_validate(False)
+
+
+def test_validate_mode_flags_duplicate_slots():
+    """Two tokens of one store that write the same slot race (a -1 slot writes
+    nothing and is never a duplicate).  Validate mode flags the race with
+    PKV_STATUS_DUP_SLOT in kv_store, qk_norm_rope_store and the fused decode
+    store, and passes the same calls once the slots are distinct."""
+    hkv, d, bs = 2, 128, 4
+    g = torch.Generator().manual_seed(77)
+    kc = torch.zeros((8, bs, hkv, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    key = torch.randn((5, hkv, d), generator=g).to(torch.bfloat16).cuda()
+    val = torch.randn((5, hkv, d), generator=g).to(torch.bfloat16).cuda()
+    q = torch.randn((5, 4, d), generator=g).to(torch.bfloat16).cuda()
+    pos = torch.arange(5, dtype=torch.int64, device="cuda")
+    w = torch.ones(d, dtype=torch.bfloat16, device="cuda")
+    dup = dev(torch.tensor([3, 9, -1, 3, -1], dtype=torch.int32))
+    distinct = dev(torch.tensor([3, 9, -1, 4, -1], dtype=torch.int32))
+    ops.set_validate(True)
+    try:
+        for call in (lambda s: ops.kv_store(key, val, kc, vc, s),
+                     lambda s: ops.qk_norm_rope_store(q, key, val, pos, w, w, kc, vc, s)):
+            with pytest.raises(ops.PagedKVError) as e:
+                call(dup)
+            assert e.value.code == 5 and "0x10" in str(e.value), str(e.value)
+            call(distinct)
+        # decode rows 0 and 2 share a table row and a context length, so
+        # their new tokens map to the same slot; row 1 is a padding row
+        bt = dev(torch.tensor([[1, 2], [-1, -1], [1, 2]], dtype=torch.int32))
+        qd = torch.randn((3, 4, d), generator=g).to(torch.bfloat16).cuda()
+        kd, vd = key[:3].contiguous(), val[:3].contiguous()
+        ctx = dev(torch.tensor([6, 0, 6], dtype=torch.int32))
+        with pytest.raises(ops.PagedKVError) as e:
+            ops.paged_attn_decode_store(qd, kd, vd, kc, vc, bt, ctx, 8)
+        assert e.value.code == 5 and "0x10" in str(e.value), str(e.value)
+        ops.paged_attn_decode_store(qd, kd, vd, kc, vc, bt, dev(torch.tensor([6, 0, 5], dtype=torch.int32)), 8)
+    finally:
+        ops.set_validate(False)
+    assert ops.device_status(clear=True) == 0
 
 
 def test_decode_step_replayed_as_cuda_graph():

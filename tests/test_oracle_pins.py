@@ -466,7 +466,8 @@ def test_prefill_rows_equal_full_prefill_rows():
 
 # ---------------------------------------------------------------------------
 # QK-Norm + RoPE prologue (L17 §4; RMSNorm module of "Nano-VLLM full-code
-# notes (5)"; rotary embedding of RoFormer §3.2)
+# notes (5)"; rotary embedding as read: split-halves pairing, e with e + d/2,
+# which the pages apply but do not print)
 # ---------------------------------------------------------------------------
 def _bf16_bits(a):
     return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16) \

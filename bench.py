@@ -479,6 +479,107 @@ def cpu_baseline_decode(work, seconds: float = 10.0, max_rows: int = 64):
     return gbs, cores, sample, el / reps
 
 
+# ---------------------------------------------------------------------------
+# secondary workloads (reported under "also"; each can run alone with --only)
+# ---------------------------------------------------------------------------
+def section_prefill_varlen(args, world, hbm, tfl):
+    """Varlen prefill step (packed k/v), 8 prompts of U[128, 4096], and the
+    kv_store of its tokens."""
+    from paged_kv_cache_303_gb300 import workloads as W
+    out = {}
+    pre = PrefillStep(W.varlen_prefill(), cache_seed=501)
+    tot, pre_ms, st_ms = time_steps(pre, args.steps, args.warmup, world, store_events=True)
+    out["prefill_varlen"] = {
+        "workload": "varlen-prefill-8x: 8 prompts U[128,4096] (%d tokens), 16q/8kv/128d" % pre.work.total_q,
+        "tflops": round(pre.flops / (pre_ms / 1e3) / 1e12, 2),
+        "kernel_ms": round(pre_ms, 4), "step_ms": round(tot / args.steps, 4),
+        "roofline": {"bound": "tensor", "peak": tfl, "unit": "TFLOP/s",
+                     "frac": round(pre.flops / (pre_ms / 1e3) / 1e12 / tfl, 4)},
+        "flops_per_launch": pre.flops,
+    }
+    out["kv_store"] = {
+        "workload": "store of the varlen-prefill step's %d tokens (D=1024)" % pre.work.total_q,
+        "gbs": round(pre.store_bytes / (st_ms / 1e3) / 1e9, 1), "kernel_ms": round(st_ms, 4),
+        "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                     "frac": round(pre.store_bytes / (st_ms / 1e3) / 1e9 / hbm, 4)},
+        "bytes_per_launch": pre.store_bytes,
+    }
+    del pre
+    torch.cuda.empty_cache()
+    return out
+
+
+def section_prologue(args, world, hbm):
+    """QK-Norm + RoPE fused with the store, on the varlen step's tokens."""
+    from paged_kv_cache_303_gb300 import workloads as W
+    pro = PrologueStep(W.varlen_prefill(), seed=511)
+    _, pro_ms, _ = time_steps(pro, args.steps, args.warmup, world)
+    out = {"qk_norm_rope_store": {
+        "workload": "QK-Norm + RoPE + K/V store of the varlen-prefill step's %d tokens "
+                    "(16q/8kv/128d, theta 1e6)" % pro.work.total_q,
+        "gbs": round(pro.bytes / (pro_ms / 1e3) / 1e9, 1), "kernel_ms": round(pro_ms, 4),
+        "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                     "frac": round(pro.bytes / (pro_ms / 1e3) / 1e9 / hbm, 4)},
+        "bytes_per_launch": pro.bytes,
+    }}
+    del pro
+    torch.cuda.empty_cache()
+    return out
+
+
+def section_prefill_prefix(args, world, tfl):
+    """Prefix-cache prefill: cached prefixes read through block_tables."""
+    from paged_kv_cache_303_gb300 import workloads as W
+    pp = PrefillStep(W.prefix_prefill(), cache_seed=601)
+    tot, pp_ms, _ = time_steps(pp, args.steps, args.warmup, world)
+    out = {"prefill_prefix": {
+        "workload": "prefix-prefill-16x: prefix U{0..12}x256 + chunk U[64,1024] (%d new tokens)" % pp.work.total_q,
+        "tflops": round(pp.flops / (pp_ms / 1e3) / 1e12, 2), "kernel_ms": round(pp_ms, 4),
+        "roofline": {"bound": "tensor", "peak": tfl, "unit": "TFLOP/s",
+                     "frac": round(pp.flops / (pp_ms / 1e3) / 1e12 / tfl, 4)},
+        "flops_per_launch": pp.flops,
+    }}
+    del pp
+    torch.cuda.empty_cache()
+    return out
+
+
+def section_decode_large(args, world, hbm):
+    """Large padded decode (GQA group 4, lognormal contexts, padding rows).
+    --large-batch / --large-pool scale it down (for profiling captures)."""
+    from paged_kv_cache_303_gb300 import workloads as W
+    batch, pool = args.large_batch, args.large_pool
+    pads = batch // 8
+    big = DecodeStep(W.large_decode(batch=batch, pads=pads, num_blocks=pool), cache_seed=701)
+    tot, big_ms, _ = time_steps(big, args.steps, args.warmup, world)
+    out = {"decode_large": {
+        "workload": f"large-decode-b{batch}p{pads}: 32q/8kv/128d, {batch}+{pads} pad rows, "
+                    f"lognormal ctx [1k,32k], {pool}-block pool",
+        "gbs": round(big.bytes / (big_ms / 1e3) / 1e9, 1), "kernel_ms": round(big_ms, 4),
+        "step_gbs": round(big.bytes / (tot / args.steps / 1e3) / 1e9, 1),
+        "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                     "frac": round(big.bytes / (big_ms / 1e3) / 1e9 / hbm, 4)},
+        "bytes_per_launch": big.bytes,
+    }}
+    del big
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_only(args, rank, world):
+    """One secondary workload alone (a short run for a profiling capture)."""
+    from paged_kv_cache_303_gb300 import build
+    build.build()
+    pk, _ = peaks()
+    hbm, tfl = float(pk["hbm_gbs"]), float(pk["bf16_tflops"])
+    fn = {"prefill_varlen": lambda: section_prefill_varlen(args, world, hbm, tfl),
+          "qk_norm_rope_store": lambda: section_prologue(args, world, hbm),
+          "prefill_prefix": lambda: section_prefill_prefix(args, world, tfl),
+          "decode_large": lambda: section_decode_large(args, world, hbm)}[args.only]
+    return {"metric": METRIC, "only": args.only, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "also": fn()}
+
+
 def run_ours(args, rank, world):
     from paged_kv_cache_303_gb300 import build, ops, workloads as W
     build.build()
@@ -558,64 +659,11 @@ def run_ours(args, rank, world):
     }
     del uf, ugraph
     torch.cuda.empty_cache()
-    # varlen prefill step (packed k/v), 8 prompts of U[128, 4096]
-    pre = PrefillStep(W.varlen_prefill(), cache_seed=501)
-    tot, pre_ms, st_ms = time_steps(pre, args.steps, args.warmup, world, store_events=True)
-    also["prefill_varlen"] = {
-        "workload": "varlen-prefill-8x: 8 prompts U[128,4096] (%d tokens), 16q/8kv/128d" % pre.work.total_q,
-        "tflops": round(pre.flops / (pre_ms / 1e3) / 1e12, 2),
-        "kernel_ms": round(pre_ms, 4), "step_ms": round(tot / args.steps, 4),
-        "roofline": {"bound": "tensor", "peak": tfl, "unit": "TFLOP/s",
-                     "frac": round(pre.flops / (pre_ms / 1e3) / 1e12 / tfl, 4)},
-        "flops_per_launch": pre.flops,
-    }
-    also["kv_store"] = {
-        "workload": "store of the varlen-prefill step's %d tokens (D=1024)" % pre.work.total_q,
-        "gbs": round(pre.store_bytes / (st_ms / 1e3) / 1e9, 1), "kernel_ms": round(st_ms, 4),
-        "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
-                     "frac": round(pre.store_bytes / (st_ms / 1e3) / 1e9 / hbm, 4)},
-        "bytes_per_launch": pre.store_bytes,
-    }
-    del pre
-    torch.cuda.empty_cache()
-    # QK-Norm + RoPE fused with the store, same tokens
-    pro = PrologueStep(W.varlen_prefill(), seed=511)
-    _, pro_ms, _ = time_steps(pro, args.steps, args.warmup, world)
-    also["qk_norm_rope_store"] = {
-        "workload": "QK-Norm + RoPE + K/V store of the varlen-prefill step's %d tokens "
-                    "(16q/8kv/128d, theta 1e6)" % pro.work.total_q,
-        "gbs": round(pro.bytes / (pro_ms / 1e3) / 1e9, 1), "kernel_ms": round(pro_ms, 4),
-        "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
-                     "frac": round(pro.bytes / (pro_ms / 1e3) / 1e9 / hbm, 4)},
-        "bytes_per_launch": pro.bytes,
-    }
-    del pro
-    torch.cuda.empty_cache()
-    # prefix-cache prefill
-    pp = PrefillStep(W.prefix_prefill(), cache_seed=601)
-    tot, pp_ms, _ = time_steps(pp, args.steps, args.warmup, world)
-    also["prefill_prefix"] = {
-        "workload": "prefix-prefill-16x: prefix U{0..12}x256 + chunk U[64,1024] (%d new tokens)" % pp.work.total_q,
-        "tflops": round(pp.flops / (pp_ms / 1e3) / 1e12, 2), "kernel_ms": round(pp_ms, 4),
-        "roofline": {"bound": "tensor", "peak": tfl, "unit": "TFLOP/s",
-                     "frac": round(pp.flops / (pp_ms / 1e3) / 1e12 / tfl, 4)},
-    }
-    del pp
-    torch.cuda.empty_cache()
-    # large padded decode
+    also.update(section_prefill_varlen(args, world, hbm, tfl))
+    also.update(section_prologue(args, world, hbm))
+    also.update(section_prefill_prefix(args, world, tfl))
     if not args.skip_large:
-        big = DecodeStep(W.large_decode(), cache_seed=701)
-        tot, big_ms, _ = time_steps(big, args.steps, args.warmup, world)
-        also["decode_large"] = {
-            "workload": "large-decode-b256p32: 32q/8kv/128d, 256+32 pad rows, lognormal ctx [1k,32k],"
-                        " 40000-block pool",
-            "gbs": round(big.bytes / (big_ms / 1e3) / 1e9, 1), "kernel_ms": round(big_ms, 4),
-            "step_gbs": round(big.bytes / (tot / args.steps / 1e3) / 1e9, 1),
-            "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
-                         "frac": round(big.bytes / (big_ms / 1e3) / 1e9 / hbm, 4)},
-        }
-        del big
-        torch.cuda.empty_cache()
+        also.update(section_decode_large(args, world, hbm))
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
@@ -709,6 +757,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-large", action="store_true")
+    ap.add_argument("--only", choices=["prefill_varlen", "qk_norm_rope_store", "prefill_prefix",
+                                       "decode_large"], default=None,
+                    help="run one secondary workload alone (for profiling captures)")
+    ap.add_argument("--large-batch", type=int, default=256)
+    ap.add_argument("--large-pool", type=int, default=40000)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -721,7 +774,7 @@ def main():
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
     rank, world, _ = dist_setup(args.gpus)
-    line = run_ours(args, rank, world)
+    line = run_only(args, rank, world) if args.only else run_ours(args, rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -223,9 +223,10 @@ int qk_norm_rope_store(const pkv_bf16 *q, int64_t q_row_stride,
  *   q    [total_q, num_heads, head_dim] bf16, row stride q_row_stride
  *   out  [total_q, num_heads, head_dim] bf16, row stride out_row_stride
  *   lse  [total_q, num_heads] fp32 or NULL
- * Supported: head_dim 128 (and 64); num_heads / num_kv_heads 1 or even;
- * with block_tables, block_size a power of two >= 8; row strides multiples
- * of 8 elements, pointers 16-byte aligned.
+ * Supported: head_dim 128 (and 64); any num_heads / num_kv_heads; with
+ * block_tables, any power-of-two block_size (blocks of 1, 2 or 4 slots are
+ * gathered row by row, larger ones by TMA boxes); row strides multiples of 8
+ * elements, pointers 16-byte aligned.
  * workspace: device scratch of at least paged_attn_prefill_workspace_size()
  * bytes (may be NULL when that is 0); its content need not be initialised.
  * ---------------------------------------------------------------------- */
@@ -266,7 +267,7 @@ size_t paged_attn_prefill_workspace_size(int32_t num_seqs, int32_t total_q,
  * which the kernel's resident CTAs claim chunks, zeroed by the call in stream
  * order, and the chunk partials); content need not be initialised.  Calls
  * that share a workspace must be ordered on the device.
- * Supported: head_dim 64 or 128; num_heads / num_kv_heads in {1,2,4,8};
+ * Supported: head_dim 64 or 128; num_heads / num_kv_heads from 1 to 8;
  * block_size a power of two.
  * ---------------------------------------------------------------------- */
 int paged_attn_decode(const pkv_bf16 *q, int64_t q_row_stride,

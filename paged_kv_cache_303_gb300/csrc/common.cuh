@@ -143,6 +143,18 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
 }
 
 // ---------------------------------------------------------------------------
+// cp.async (16-byte pieces, global -> shared, L2 only); src_bytes 0
+// zero-fills the destination without reading the source.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// ---------------------------------------------------------------------------
 // Non-coherent streaming loads (data read once), plain vector stores.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
@@ -165,6 +177,40 @@ __device__ __forceinline__ void st_cs_v4(void *p, uint4 v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
                  : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core products (mma.sync m16n8k16, bf16 inputs, fp32
+// accumulators) and the shared-memory fragment loads that feed them.  For a
+// lane, g = lane / 4 and t = lane % 4:
+//   A (16 x 16, row-major): a[0] = (row g,   cols 2t, 2t+1), a[1] = (row g+8, same cols),
+//                           a[2] = (row g,   cols 8+2t, +1), a[3] = (row g+8, cols 8+2t, +1)
+//   B (16 x 8, k x n):      b[0] = (k 2t, 2t+1; col g),       b[1] = (k 8+2t, +1; col g)
+//   D (16 x 8, fp32):       d[0], d[1] = (row g, cols 2t, 2t+1), d[2], d[3] = (row g+8, same)
+// (the lower-indexed element of a pair in the low 16 bits).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// four 8x8 b16 matrices; lanes 8i .. 8i+7 give the row addresses of matrix i
+// and r[i] receives (row lane/4, cols 2(lane%4), +1) of matrix i
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// the same, transposed: r[i] receives (rows 2(lane%4), +1; col lane/4) of matrix i
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
 }
 
 // three-input maximum (one instruction on sm_100 and later)

@@ -6,8 +6,8 @@
 // Work items: (chunk of keys, sequence, kv head).  A CTA works on one item
 // at a time with the GQA group's G query vectors (all query heads that share
 // the kv head, §3) in shared memory, so every K/V byte it reads serves G
-// heads.  The CTAs are persistent -- one resident wave, four per SM (128
-// registers a thread) -- and claim items from a counter in the workspace,
+// heads.  The CTAs are persistent -- one resident wave, six per SM (shared
+// memory the limit) -- and claim items from a counter in the workspace,
 // chunk index outermost, so the full chunks are taken before the short last
 // chunks of each sequence.
 //
@@ -17,23 +17,27 @@
 //     (box: 64 head_dim elements x 1 head x min(block_size, 32) slots).  With
 //     block_size >= 8 the boxes use the 128-byte swizzle so that the
 //     row-per-lane reads below are bank-conflict free.
-//   * One producer warp claims items, writes each item's record and scaled
-//     query vectors into a two-entry item queue, and keeps a 3-stage tile
-//     ring full (an mbarrier pair per stage) across item boundaries, so the
-//     next item's first tiles are in flight while the consumers merge the
-//     current one.  Two consumer warps (kConsumers) take the queue's items
+//   * One producer warp claims items, writes each item's record and query
+//     vectors into a two-entry item queue, and keeps a 2-stage tile ring
+//     full (an mbarrier pair per stage) across item boundaries, so the next
+//     item's first tile is in flight while the consumer merges the current
+//     one.  kConsumers consumer warps (one by default) take the queue's items
 //     in order; tile i of an item goes to warp i % kConsumers, with no
 //     CTA-wide barrier inside the tile loop.
-//   * Scores: lane = token; the lane dots its key row with the G queries
-//     (packed fp32x2 FMAs).  Scores carry scale*log2(e) so the softmax uses
-//     exp2.
+//   * Scores and P.V are warp-wide tensor-core products (mma.sync, bf16
+//     inputs, fp32 accumulators): S = q K^T with the group's heads as rows,
+//     then O^T += V^T P^T with the probabilities kept in the registers the
+//     scores came out in.  Scores carry scale*log2(e) so the softmax uses
+//     exp2.  (The two products are small -- G heads by 32 tokens -- and the
+//     kernel stays HBM-bound; the tensor cores take the instruction count per
+//     tile from about 1800 to about 200, which is what limited it.)
 //   * Softmax: per warp and head, the tile maximum (shuffles) updates the
 //     warp's running maximum m; its running sum l and output accumulators are
 //     rescaled by 2^(m_old-m_new) (§5.2's exact rescaling).
-//   * P.V: lane = head_dim/32 elements of every value row; in a tile that is
-//     not complete (sequence tail, missing block) tokens whose probabilities
-//     are all zero are skipped, so garbage in unwritten cache slots never
-//     reaches the sum.
+//   * In a tile that is not complete (sequence tail, missing block) tokens
+//     that are not valid get probability 0 and their value rows are zeroed
+//     in registers, so garbage in unwritten cache slots never reaches the
+//     sum.
 //   * Fused store (paged_attn_decode_store): for the item whose chunk holds
 //     position ctx-1 the producer warp first writes the step's new K/V row
 //     of its kv head to that slot (the decode slot of Lesson 04 §4) with
@@ -51,7 +55,13 @@
 //     form 5.33 (per-item start-up hidden behind the previous item); on it,
 //     two consumer warps per CTA instead of three (cheaper merges, more
 //     CTAs' producers in flight) 5.36 -> 5.52, and 4.93 -> 5.08 on the
-//     large batch-256 workload.
+//     large batch-256 workload.  The CUDA-core products were issue-bound
+//     (ncu on the group-4 workload: 45 % issue-active, 51 % DRAM-active);
+//     with the tensor-core products the step (CUDA graph) went from 5.66 to
+//     6.02 TB/s and the group-4 decode from 4.98 to 6.90 TB/s; consumers x
+//     stages x CTAs/SM then: 2x3x5 6.02 / 6.90, 1x3x8 5.97 / 6.91, 1x4x6
+//     5.89 / 6.82, 2x4x4 5.78 / 6.76, 1x2x8 6.06 / 6.92 (kept), 2x2x6 5.45 /
+//     6.79.
 //
 // Bound: HBM.  Algorithmic bytes per launch = sum_b ctx_b * Hkv * d * 2 * 2
 // (K and V, bf16) + q and out; arithmetic intensity about G FLOP/byte.
@@ -96,13 +106,13 @@ namespace {
 
 // Tunables (compile-time): consumer warps per CTA, ring depth, CTAs per SM.
 #ifndef PKV_DEC_CONSUMERS
-#define PKV_DEC_CONSUMERS 2
+#define PKV_DEC_CONSUMERS 1
 #endif
 #ifndef PKV_DEC_STAGES
-#define PKV_DEC_STAGES 3
+#define PKV_DEC_STAGES 2
 #endif
 #ifndef PKV_DEC_MIN_CTAS
-#define PKV_DEC_MIN_CTAS 5
+#define PKV_DEC_MIN_CTAS 8
 #endif
 constexpr int kConsumers = PKV_DEC_CONSUMERS;    // consumer warps per CTA
 constexpr int kThreads = (kConsumers + 1) * 32;  // + one TMA producer warp
@@ -205,9 +215,10 @@ struct Layout {
     static constexpr int kPipeBytes = kStages * kStageBytes;
     static constexpr int kOffBar = kPipeBytes;      // full[S] empty[S] ready[Q] free[Q] masks abort
     static constexpr int kOffItems = kOffBar + 256; // ItemRec[kQ], then two decision words
-    static constexpr int kOffQ = kOffItems + 128;   // q (scaled fp32) [kQ][G][HD]; merge buffer
-    static constexpr int kOffP = kOffQ + kQ * G * HD * 4;            // [warp][G][kTile]
-    static constexpr int kOffML = kOffP + kConsumers * G * kTile * 4; // [warp][G][2]
+    // per queue entry: q as bf16 [G][HD] in the first half, later the fp32
+    // merge buffer [G][HD]
+    static constexpr int kOffQ = kOffItems + 128;
+    static constexpr int kOffML = kOffQ + kQ * G * HD * 4;           // [warp][G][2]
     static constexpr int kBytes = kOffML + kConsumers * G * 2 * 4;
     static_assert(2 * kStages * 8 + 2 * kQ * 8 + kStages * 4 + 4 <= 256, "barrier area");
     static_assert(kQ * (int)sizeof(ItemRec) + 8 <= 128, "item area");
@@ -236,7 +247,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     // that every consumer warp takes the same path through the barriers
     int *decide = reinterpret_cast<int *>(smem + L::kOffItems + kQ * sizeof(ItemRec));
     float *qring = reinterpret_cast<float *>(smem + L::kOffQ);
-    float *ps = reinterpret_cast<float *>(smem + L::kOffP);
     float *mml = reinterpret_cast<float *>(smem + L::kOffML);
 
     const int tid = threadIdx.x;
@@ -344,19 +354,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
                 break;
             }
-            // the item's G query vectors, scaled by scale*log2(e), as fp32
-            float *qd = qring + e * G * HD;
+            // the item's G query vectors (bf16, as given) into the queue entry
+            uint4 *qd = reinterpret_cast<uint4 *>(qring + e * G * HD);
             for (int c = lane; c < G * HD / 8; c += 32) {
                 const int h = c / (HD / 8), cc = c % (HD / 8);
-                const uint4 w = *reinterpret_cast<const uint4 *>(p.q + (int64_t)it.b * p.q_rs +
-                                                                 (int64_t)(it.kvh * G + h) * HD + cc * 8);
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-                float *dst = qd + h * HD + cc * 8;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    dst[2 * k] = bf16lo_to_f32(ws[k]) * p.scale_log2;
-                    dst[2 * k + 1] = bf16hi_to_f32(ws[k]) * p.scale_log2;
-                }
+                qd[c] = *reinterpret_cast<const uint4 *>(p.q + (int64_t)it.b * p.q_rs +
+                                                         (int64_t)(it.kvh * G + h) * HD + cc * 8);
             }
             __syncwarp();
             if (lane == 0) {
@@ -421,13 +424,40 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     }
 
     // ----------------------------------------------------------------------
-    // consumer warps: items in queue order
+    // consumer warps: items in queue order.  The two products of a tile run
+    // on the tensor cores as warp-wide mma.sync (m16n8k16, bf16 inputs, fp32
+    // accumulators); a lane holds fragments, g = lane / 4, t = lane % 4:
+    //   S = q K^T    M = query heads of the group (G <= 8 real rows of 16),
+    //                N = 8 tokens per product, K = 16 head_dim elements;
+    //                q (A) stays in registers for the item, K (B) comes from
+    //                the ring by ldmatrix.  Lane (g, t) holds the scores of
+    //                head g for tokens 8n + 2t, 8n + 2t + 1 (n = 0..3).
+    //   O^T += V^T P^T   M = 16 head_dim elements, N = 8 heads, K = 16
+    //                tokens; V^T (A) comes from the ring by ldmatrix.trans,
+    //                and the score fragments, turned into bf16 probabilities,
+    //                are exactly the B fragments (P^T), so P never leaves
+    //                registers.  Lane (g, t) accumulates O of heads 2t, 2t+1
+    //                at head_dim elements 16m + g and 16m + g + 8.
+    // Softmax per head over the tile: the 4 lanes of a group hold the head's
+    // 32 scores (8 each); two xor shuffles give the tile maximum.  Tokens
+    // that are not valid (sequence tail, missing block) get probability 0
+    // and their value rows are zeroed in registers, so unwritten cache slots
+    // never reach the sum.  The running sum l adds the probabilities as
+    // rounded to bf16 for the product, so numerator and denominator use the
+    // same weights.
     // ----------------------------------------------------------------------
-    float *pw = ps + warp * G * kTile;             // this warp's probabilities [G][kTile]
-    const int v_half = (lane * DPL) / 64;
-    const int v_chunk = ((lane * DPL) % 64) / 8;
-    const int v_byte = ((lane * DPL) % 8) * 2;
+    constexpr int KS = HD / 16;                    // 16-element steps over head_dim
+    const int gq = lane >> 2, tq = lane & 3;
+    const bool real_head = gq < G;
+    // ldmatrix: lane 8i + r addresses row r of matrix i; matrices 0,1 cover
+    // tokens 0..7 and 2,3 tokens 8..15 of a 16-token block, even / odd
+    // 16-byte chunks
+    const int lm_row = ((lane >> 4) << 3) + (lane & 7);
+    const int lm_odd = (lane >> 3) & 1;
     const uint32_t all_segs = kTile / TB >= 32 ? 0xffffffffu : ((1u << (kTile / TB)) - 1u);
+    auto frag_addr = [&](uint32_t tile_base, int row, int chunk) -> uint32_t {
+        return tile_base + (uint32_t)((chunk >> 3) * kTile * 128) + chunk_off<SW>(row, chunk & 7);
+    };
     int g0 = 0;
     for (int seq = 0;; ++seq) {
         const int e = seq % kQ;
@@ -442,15 +472,20 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         const float *qs = qring + e * G * HD;
         const int hq0 = it.kvh * G;
 
-        float m_run[G], l_part[G];
-        float2 o2[G][DPL / 2];
+        // q fragments of head gq (rows gq + 8 are zero)
+        uint32_t qa[KS][2];
+        {
+            const uint16_t *qrow = reinterpret_cast<const uint16_t *>(qs) + gq * HD + 2 * tq;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            m_run[h] = -INFINITY;
-            l_part[h] = 0.f;
-#pragma unroll
-            for (int k = 0; k < DPL / 2; ++k) o2[h][k] = make_float2(0.f, 0.f);
+            for (int kk = 0; kk < KS; ++kk) {
+                qa[kk][0] = real_head ? *reinterpret_cast<const uint32_t *>(qrow + kk * 16) : 0u;
+                qa[kk][1] = real_head ? *reinterpret_cast<const uint32_t *>(qrow + kk * 16 + 8) : 0u;
+            }
         }
+        float m_run = -INFINITY, l_part = 0.f;      // head gq
+        float o[KS][4];                             // O^T fragments
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         bool live = true;
         for (int i = warp; i < it.ntiles; i += kConsumers) {
             const int gt = g0 + i;
@@ -466,107 +501,94 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                 live = false;
                 break;
             }
-            const unsigned char *ktile = pipe + stage * L::kStageBytes;
-            const unsigned char *vtile = ktile + L::kTileBytes;
+            const uint32_t kbase = smem_u32(pipe + stage * L::kStageBytes);
+            const uint32_t vbase = kbase + L::kTileBytes;
             const int p0 = it.tok_begin + i * kTile;
-
-            // ---- scores: lane = token ----
-            float2 acc[G][2];
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[h][0] = acc[h][1] = make_float2(0.f, 0.f);
-#pragma unroll 4
-            for (int c = 0; c < CPR; ++c) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(ktile + (c / 8) * kTile * 128 +
-                                                                 chunk_off<SW>(lane, c % 8));
-                const float2 k0 = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
-                const float2 k1 = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
-                const float2 k2 = make_float2(bf16lo_to_f32(w.z), bf16hi_to_f32(w.z));
-                const float2 k3 = make_float2(bf16lo_to_f32(w.w), bf16hi_to_f32(w.w));
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float4 qa = *reinterpret_cast<const float4 *>(qs + h * HD + c * 8);
-                    const float4 qb = *reinterpret_cast<const float4 *>(qs + h * HD + c * 8 + 4);
-                    acc[h][0] = ffma2(make_float2(qa.x, qa.y), k0, acc[h][0]);
-                    acc[h][1] = ffma2(make_float2(qa.z, qa.w), k1, acc[h][1]);
-                    acc[h][0] = ffma2(make_float2(qb.x, qb.y), k2, acc[h][0]);
-                    acc[h][1] = ffma2(make_float2(qb.z, qb.w), k3, acc[h][1]);
-                }
-            }
             const uint32_t mask = seg_valid[stage];
-            const bool valid = (p0 + lane < it.tok_end) && ((mask >> (lane / TB)) & 1u);
             const bool full_tile = (p0 + kTile <= it.tok_end) && mask == all_segs;
 
-            // ---- online softmax over the warp's tile ----
-            float alpha[G];
+            // ---- S = q K^T ----
+            float s[4][4];
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float s = valid ? (acc[h][0].x + acc[h][0].y) + (acc[h][1].x + acc[h][1].y)
-                                      : -INFINITY;
-                float mt = s;
+            for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-                const float m_new = fmaxf(m_run[h], mt);
-                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                alpha[h] = fast_exp2(m_run[h] - m_use);
-                m_run[h] = m_new;
-                const float pr = fast_exp2(s - m_use);
-                l_part[h] = l_part[h] * alpha[h] + pr;
-                pw[h * kTile + lane] = pr;
+            for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+                for (int np = 0; np < 2; ++np) {
+                    uint32_t b[4];
+                    ldmatrix_x4(b, frag_addr(kbase, np * 16 + lm_row, 2 * kk + lm_odd));
+                    mma_bf16_16816(s[2 * np], qa[kk][0], 0u, qa[kk][1], 0u, b[0], b[1]);
+                    mma_bf16_16816(s[2 * np + 1], qa[kk][0], 0u, qa[kk][1], 0u, b[2], b[3]);
+                }
             }
-            __syncwarp();
-
-            // ---- P.V: lane = DPL head_dim elements ----
+            // scores in exp2 units; padding heads keep 0 (finite, unused)
+            float sc[8];
 #pragma unroll
-            for (int h = 0; h < G; ++h)
+            for (int nt = 0; nt < 4; ++nt) {
+                sc[2 * nt] = real_head ? s[nt][0] * p.scale_log2 : 0.f;
+                sc[2 * nt + 1] = real_head ? s[nt][1] * p.scale_log2 : 0.f;
+            }
+            if (!full_tile && real_head) {
 #pragma unroll
-                for (int k = 0; k < DPL / 2; ++k) o2[h][k] = fmul2(o2[h][k], make_float2(alpha[h], alpha[h]));
-            const unsigned char *vrow0 = vtile + v_half * kTile * 128 + v_byte;
-            auto pv_token = [&](int t, const float (&pr)[G]) {
-                const unsigned char *src = vrow0 + chunk_off<SW>(t, v_chunk);
-                if constexpr (DPL == 4) {
-                    const uint2 w = *reinterpret_cast<const uint2 *>(src);
-                    const float2 v0 = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
-                    const float2 v1 = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float2 pp = make_float2(pr[h], pr[h]);
-                        o2[h][0] = ffma2(pp, v0, o2[h][0]);
-                        o2[h][1] = ffma2(pp, v1, o2[h][1]);
-                    }
-                } else {
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
-                    const float2 v0 = make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w));
-#pragma unroll
-                    for (int h = 0; h < G; ++h) o2[h][0] = ffma2(make_float2(pr[h], pr[h]), v0, o2[h][0]);
+                for (int u = 0; u < 8; ++u) {
+                    const int tk = (u >> 1) * 8 + 2 * tq + (u & 1);
+                    const bool ok = (p0 + tk < it.tok_end) && ((mask >> (tk / TB)) & 1u);
+                    if (!ok) sc[u] = -INFINITY;
                 }
-            };
-            if (full_tile) {
-#pragma unroll 2
-                for (int t4 = 0; t4 < kTile; t4 += 4) {
-                    float4 pq[G];
+            }
+            // ---- online softmax of head gq over the tile ----
+            float mt = fmax3(fmax3(sc[0], sc[1], sc[2]), fmax3(sc[3], sc[4], sc[5]), fmaxf(sc[6], sc[7]));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+            const float m_new = fmaxf(m_run, mt);
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = fast_exp2(m_run - m_use);
+            m_run = m_new;
+            uint32_t pb[2][2];                      // P^T fragments, 16-token steps
+            float lsum = 0.f;
 #pragma unroll
-                    for (int h = 0; h < G; ++h) pq[h] = *reinterpret_cast<const float4 *>(pw + h * kTile + t4);
+            for (int nt = 0; nt < 4; ++nt) {
+                const uint32_t pk = pack_bf16x2(fast_exp2(sc[2 * nt] - m_use), fast_exp2(sc[2 * nt + 1] - m_use));
+                pb[nt >> 1][nt & 1] = pk;
+                lsum += bf16lo_to_f32(pk) + bf16hi_to_f32(pk);
+            }
+            l_part = l_part * alpha + lsum;
+            // rescale the accumulators of heads 2t, 2t+1
+            const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * tq) * 4);
+            const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * tq + 1) * 4);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        float pr[G];
+            for (int m2 = 0; m2 < KS; ++m2) {
+                o[m2][0] *= a0;
+                o[m2][1] *= a1;
+                o[m2][2] *= a0;
+                o[m2][3] *= a1;
+            }
+            // ---- O^T += V^T P^T ----
+            // value rows of tokens that are not valid: zeroed in the fragments
+            uint32_t vmask[2][2] = {{0xffffffffu, 0xffffffffu}, {0xffffffffu, 0xffffffffu}};
+            if (!full_tile) {
 #pragma unroll
-                        for (int h = 0; h < G; ++h)
-                            pr[h] = u == 0 ? pq[h].x : u == 1 ? pq[h].y : u == 2 ? pq[h].z : pq[h].w;
-                        pv_token(t4 + u, pr);
+                for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t m2 = 0u;
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int tk = kt * 16 + hh * 8 + 2 * tq + u;
+                            const bool ok = (p0 + tk < it.tok_end) && ((mask >> (tk / TB)) & 1u);
+                            if (ok) m2 |= 0xffffu << (16 * u);
+                        }
+                        vmask[kt][hh] = m2;
                     }
-                }
-            } else {
-                // sequence tail or missing segment: skip tokens whose
-                // probabilities are all zero
-                for (int t = 0; t < kTile; ++t) {
-                    float pr[G];
-                    bool any = false;
+            }
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        pr[h] = pw[h * kTile + t];
-                        any |= pr[h] != 0.f;
-                    }
-                    if (any) pv_token(t, pr);        // warp-uniform
+            for (int kt = 0; kt < 2; ++kt) {
+#pragma unroll
+                for (int m2 = 0; m2 < KS; ++m2) {
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(a, frag_addr(vbase, kt * 16 + lm_row, 2 * m2 + lm_odd));
+                    mma_bf16_16816(o[m2], a[0] & vmask[kt][0], a[1] & vmask[kt][0], a[2] & vmask[kt][1],
+                                   a[3] & vmask[kt][1], pb[kt][0], pb[kt][1]);
                 }
             }
             __syncwarp();
@@ -574,46 +596,52 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         }
 
         // ---- merge the consumer warps' states, in warp order ----
-        // (the item's query vectors are no longer needed: their smem takes
-        // the merged output)
+        // (the item's q is in registers: its smem takes the merged output)
         consumer_sync();
         (void)live;
         if (tid == 0) decide[1] = *abort_flag;      // read once, seen by all after the barrier
-        float *ob = const_cast<float *>(qs);            // [G][HD]
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float l = l_part[h];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-            if (lane == 0) {
-                mml[(warp * G + h) * 2] = m_run[h];
-                mml[(warp * G + h) * 2 + 1] = l;
+        float *ob = const_cast<float *>(qs);        // [G][HD]
+        {
+            float l = l_part;
+            l += __shfl_xor_sync(0xffffffffu, l, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            if (tq == 0 && real_head) {
+                mml[(warp * G + gq) * 2] = m_run;
+                mml[(warp * G + gq) * 2 + 1] = l;
             }
         }
         consumer_sync();
         const bool aborted = decide[1] != 0;        // uniform
-        float f_own[G];
+        // this warp's factor for the heads 2t, 2t+1 of its fragments
+        float f_own[2];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float m = -INFINITY;
+        for (int u = 0; u < 2; ++u) {
+            const int h = 2 * tq + u;
+            f_own[u] = 0.f;
+            if (h < G) {
+                float m = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kConsumers; ++w) m = fmaxf(m, mml[(w * G + h) * 2]);
-            const float mu = (m == -INFINITY) ? 0.f : m;
-            f_own[h] = fast_exp2(m_run[h] - mu);
+                for (int w = 0; w < kConsumers; ++w) m = fmaxf(m, mml[(w * G + h) * 2]);
+                const float mu = (m == -INFINITY) ? 0.f : m;
+                f_own[u] = fast_exp2(mml[(warp * G + h) * 2] - mu);
+            }
         }
 #pragma unroll 1
         for (int w = 0; w < kConsumers; ++w) {
             if (warp == w) {
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float *dst = ob + h * HD + lane * DPL;
+                for (int m2 = 0; m2 < KS; ++m2)
 #pragma unroll
-                    for (int k = 0; k < DPL / 2; ++k) {
-                        const float ox = f_own[h] * o2[h][k].x, oy = f_own[h] * o2[h][k].y;
-                        dst[2 * k] = (w == 0 ? 0.f : dst[2 * k]) + ox;
-                        dst[2 * k + 1] = (w == 0 ? 0.f : dst[2 * k + 1]) + oy;
-                    }
-                }
+                    for (int r = 0; r < 2; ++r)
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int h = 2 * tq + u;
+                            if (h < G) {
+                                float *dst = ob + h * HD + m2 * 16 + gq + 8 * r;
+                                const float v = f_own[u] * o[m2][2 * r + u];
+                                *dst = (w == 0 ? 0.f : *dst) + v;
+                            }
+                        }
             }
             consumer_sync();
         }
@@ -726,9 +754,13 @@ int dispatch_group(int G, const CUtensorMap &km, const CUtensorMap &vm, const De
     switch (G) {
         case 1: return launch_split<HD, 1, SW>(km, vm, p, batch, hkv, s, err);
         case 2: return launch_split<HD, 2, SW>(km, vm, p, batch, hkv, s, err);
+        case 3: return launch_split<HD, 3, SW>(km, vm, p, batch, hkv, s, err);
         case 4: return launch_split<HD, 4, SW>(km, vm, p, batch, hkv, s, err);
+        case 5: return launch_split<HD, 5, SW>(km, vm, p, batch, hkv, s, err);
+        case 6: return launch_split<HD, 6, SW>(km, vm, p, batch, hkv, s, err);
+        case 7: return launch_split<HD, 7, SW>(km, vm, p, batch, hkv, s, err);
         case 8: return launch_split<HD, 8, SW>(km, vm, p, batch, hkv, s, err);
-        default: *err = "num_heads / num_kv_heads must be 1, 2, 4 or 8"; return PKV_ERR_UNSUPPORTED;
+        default: *err = "num_heads / num_kv_heads must be 1 to 8"; return PKV_ERR_UNSUPPORTED;
     }
 }
 

@@ -7,7 +7,8 @@
 //
 // Work unit: one CTA per (128 query rows of one sequence, two query heads of
 // one GQA group).  The two heads share every K/V tile the CTA loads, which
-// halves K/V traffic per FLOP compared with one head per CTA.
+// halves K/V traffic per FLOP compared with one head per CTA.  When the
+// group size is odd a CTA takes one head (the second softmax warpgroup idles).
 //
 // Roles (320 threads):
 //   warps 0-3  softmax warpgroup of query head A, thread = query row = TMEM lane
@@ -15,7 +16,8 @@
 //   warp 8     TMA producer: Q once, then K_0, V_0, K_1, ... (128 keys each)
 //              through a ring of kSlots tiles (packed k/v: one box per 64
 //              columns of head_dim; paged cache: one box per block segment,
-//              addressed via block_tables)
+//              addressed via block_tables; blocks shorter than 8 rows are
+//              copied row by row with cp.async into the same layout)
 //   warp 9     MMA issuer (one lane): S_A(0), S_B(0), then per key tile j
 //              P_A(j) V_j, S_A(j+1), P_B(j) V_j, S_B(j+1), so the tensor core
 //              works on one head while the other head's softmax runs
@@ -272,6 +274,10 @@ struct PrefillParams {
     const int32_t *work_count;   // [1]
     const int2 *work;            // [max_items] (sequence, 128-row block)
     int32_t max_items;
+    // paged mode with blocks shorter than the 8-row swizzle atom: K/V tiles
+    // are copied row by row from the caches instead of by TMA boxes
+    int32_t row_copy;
+    const uint16_t *k_cache, *v_cache;
 };
 
 __device__ __forceinline__ int kv_tiles_for(int Lq, int Lk, int mb) {
@@ -414,7 +420,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int r0 = mb * kBM;
     const int n_kv = kv_tiles_for(Lq, Lk, mb);
     const int G = p.num_heads / p.num_kv_heads;
-    const int ntile = G >= 2 ? 2 : 1;
+    const int ntile = G % 2 == 0 ? 2 : 1;        // two heads of one group, or one head
     const int h0 = blockIdx.x * ntile;
     const int kvh = h0 / G;
 
@@ -427,7 +433,85 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         return;
     }
 
-    if (warp == kProducerWarp) {
+    if (warp == kProducerWarp && p.row_copy) {
+        // ------------------------------------------------------------------
+        // Producer for paged caches whose blocks are shorter than the 8-row
+        // swizzle atom (block_size 1, 2, 4): Q by TMA as usual; each K / V
+        // tile is copied by the whole warp in 16-byte pieces with cp.async,
+        // row by row through block_tables, into the same 128-byte-swizzled
+        // layout a TMA box writes.  Rows past the last key and rows of
+        // missing blocks are zero-filled, so the final tile needs no fix-up.
+        // A tile is published (slot_full) once the next one is in flight:
+        // every lane waits for its own pieces, fences them into the async
+        // proxy that the tensor core reads through, then lane 0 arrives.
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            const uint64_t pol_stream = policy_evict_first();
+            mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * L::kQTile));
+            for (int t = 0; t < ntile; ++t)
+                for (int hf = 0; hf < H; ++hf)
+                    tma_load_3d(smem + t * L::kQTile + hf * kBM * 128, &qmap, q_full, hf * 64, h0 + t,
+                                q0 + r0, pol_stream);
+        }
+        constexpr int CPR = HD / 8;                  // 16-byte pieces per row
+        const int bs = p.block_size;
+        const int32_t *bt_row = p.bt + (int64_t)seq * p.bt_stride;
+        const int64_t row_elems = (int64_t)p.num_kv_heads * HD;
+        bool live = true;
+        int n = 0;
+        for (; n < 2 * n_kv; ++n) {
+            const int s = n % kSlots;
+            const int j = n >> 1;
+            const uint16_t *cache = (n & 1) ? p.v_cache : p.k_cache;
+            if (n >= kSlots) {
+                int ok = 1;
+                if (lane == 0)
+                    ok = wait_or_abort(&slot_free[s], (uint32_t)((n / kSlots) - 1) & 1u, abort_flag) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    live = false;
+                    break;
+                }
+            }
+            const uint32_t dst = smem_u32(smem + L::kOffRing + s * L::kKVTile);
+            bool missing = false;
+            for (int pc = lane; pc < kBN * CPR; pc += 32) {
+                const int r = pc / CPR, cc = pc % CPR;
+                const int pos = j * kBN + r;
+                const uint16_t *src = cache;
+                uint32_t nbytes = 0;
+                if (pos < Lk) {
+                    const int lb = pos / bs;
+                    const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
+                    if (blk >= 0 && blk < p.num_blocks) {
+                        src = cache + ((int64_t)blk * bs + pos % bs) * row_elems + (int64_t)kvh * HD + cc * 8;
+                        nbytes = 16;
+                    } else {
+                        missing = true;
+                    }
+                }
+                cp_async16(dst + (uint32_t)((cc / 8) * (kBN * 128) + r * 128 + (((cc % 8) ^ (r & 7)) << 4)),
+                           src, nbytes);
+            }
+            cp_async_commit();
+            if (missing && !(n & 1)) atomicOr(&g_prefill_status, PKV_STATUS_BAD_BLOCK);
+            if (n > 0) {
+                cp_async_wait<1>();                  // this lane's pieces of tile n-1 landed
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&slot_full[(n - 1) % kSlots]);
+            }
+        }
+        cp_async_wait<0>();                          // nothing may land after the CTA leaves
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (live && n > 0) {
+                mbar_arrive(&slot_full[(n - 1) % kSlots]);
+                if (n_kv * kBN > Lk) mbar_arrive(v_fix);   // the tail rows are zeros already
+            }
+            (void)mbar_wait(q_full, 0);
+        }
+    } else if (warp == kProducerWarp) {
         // ------------------------------------------------------------------
         // TMA producer: Q, then the loads K_0, V_0, K_1, V_1, ... into a
         // ring of kSlots tiles (load n -> slot n % kSlots)
@@ -731,7 +815,7 @@ int launch_hd(const PrefillArgs &a, const PrefillParams &pp, int2 *work, int32_t
         });
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
     const int G = a.num_heads / a.num_kv_heads;
-    const int ntile = G >= 2 ? 2 : 1;
+    const int ntile = G % 2 == 0 ? 2 : 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.num_heads / ntile, max_items);
     cfg.blockDim = dim3(kThreads);
@@ -766,14 +850,9 @@ int launch_prefill(const PrefillArgs &a, cudaStream_t stream, const char **err) 
         *err = "head_dim must be 64 or 128";
         return PKV_ERR_UNSUPPORTED;
     }
-    const int G = a.num_heads / a.num_kv_heads;
-    if (G > 1 && G % 2) {
-        *err = "num_heads / num_kv_heads must be 1 or even";
-        return PKV_ERR_UNSUPPORTED;
-    }
     const bool paged = a.bt != nullptr;
-    if (paged && (a.block_size < 8 || (a.block_size & (a.block_size - 1)))) {
-        *err = "paged prefill needs a power-of-two block_size >= 8";
+    if (paged && (a.block_size < 1 || (a.block_size & (a.block_size - 1)))) {
+        *err = "paged prefill needs a power-of-two block_size";
         return PKV_ERR_UNSUPPORTED;
     }
     const size_t need = prefill_workspace_bytes(a.num_seqs, a.total_q, a.max_seqlen_q, a.num_heads);
@@ -807,6 +886,9 @@ int launch_prefill(const PrefillArgs &a, cudaStream_t stream, const char **err) 
     pp.work_count = count;
     pp.work = work;
     pp.max_items = max_items;
+    pp.row_copy = paged && a.block_size < 8 ? 1 : 0;
+    pp.k_cache = a.k_cache;
+    pp.v_cache = a.v_cache;
     if (a.head_dim == 128) return launch_hd<128>(a, pp, work, count, max_items, stream, err);
     return launch_hd<64>(a, pp, work, count, max_items, stream, err);
 }

@@ -213,6 +213,11 @@ DECODE_SHAPES = [
     (16, 2, 128, 64, [65, 640, 1]),
     (8, 1, 64, 32, [300, 31, 32]),
     (16, 8, 128, 16, [0, 5, 0, 200, 1]),      # one chunk per row, padding rows
+    # GQA groups 3, 5, 6, 7 (odd groups and a group that is not a power of two)
+    (12, 4, 128, 256, [700, 1, 256, 2500]),
+    (10, 2, 64, 16, [90, 333, 0]),
+    (12, 2, 128, 32, [64, 1025]),
+    (14, 2, 128, 256, [513, 7]),
 ]
 
 
@@ -235,10 +240,21 @@ def test_decode_other_block_sizes(bs):
     _decode_case(W.Heads(16, 4, 128, bs, need), ctx, seed=340 + bs)
 
 
-@pytest.mark.parametrize("bs", [8, 128])
+@pytest.mark.parametrize("bs", [1, 2, 4, 8, 128])
 def test_prefill_prefix_cache_other_block_sizes(bs):
+    """Block sizes 1, 2 and 4 (shorter than the 8-row swizzle atom: tiles
+    gathered row by row) next to 8 and 128 (TMA boxes per block), with
+    prefixes that end mid-block and NaN in every slot no row reads."""
     heads = W.Heads(16, 8, 128, bs, 96 * 256 // bs)
     _prefill_paged(heads, [100, 257, 7], [bs + 5, 3, 2 * bs], seed=790 + bs)
+
+
+@pytest.mark.parametrize("bs", [1, 2, 4])
+def test_prefill_small_blocks_d64_group4_growing_scores(bs):
+    heads = W.Heads(16, 4, 64, bs, 64 * 64 // bs)
+    _prefill_paged(heads, [300, 129, 1], [77, 0, 130], seed=820 + bs)
+    heads = W.Heads(16, 8, 128, bs, 96 * 64 // bs)
+    _prefill_paged(heads, [400, 60], [3 * 128 + 1, 5], seed=830 + bs, growing=True)
 
 
 def test_decode_tiny_pipeline():
@@ -445,10 +461,19 @@ def test_prefill_prefix_cache_aligned(bs):
     _prefill_paged(heads, [100, 300, 1, 64], [2 * bs, 0, 3 * bs, bs], seed=700 + bs)
 
 
-@pytest.mark.parametrize("bs", [16, 256])
+@pytest.mark.parametrize("bs", [4, 16, 256])
 def test_prefill_prefix_cache_unaligned(bs):
     heads = W.Heads(16, 8, 128, bs, 96 * 256 // bs)
     _prefill_paged(heads, [100, 257, 7], [bs + 5, 3, 2 * bs + bs - 1], seed=750 + bs)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(12, 4, 128), (10, 2, 64), (7, 1, 128)])
+def test_prefill_odd_groups(hq, hkv, d):
+    """GQA groups 3, 5 and 7: one head per CTA; packed and prefix-cache
+    prefill both against the oracle."""
+    _prefill_packed(W.Heads(hq, hkv, d, 16, 256), [1, 129, 300, 77], seed=640 + hq)
+    heads = W.Heads(hq, hkv, d, 32, 64)
+    _prefill_paged(heads, [150, 40], [64 + 3, 0], seed=650 + hq)
 
 
 def test_prefill_paged_group4_d64():

@@ -566,13 +566,33 @@ def section_decode_large(args, world, hbm):
     return out
 
 
+def section_decode(args, world, hbm):
+    """The headline decode step (paged_attn_decode_store + merge) launched
+    eagerly, alone."""
+    from paged_kv_cache_303_gb300 import workloads as W
+    dec = DecodeStep(W.qwen3_decode(), cache_seed=401, fused=True)
+    _, k_ms, _ = time_steps(dec, args.steps, args.warmup, world)
+    alg = dec.bytes + dec.qo_bytes + dec.store_bytes
+    out = {"decode": {
+        "workload": "qwen3-decode-b64, paged_attn_decode_store + merge, eager",
+        "gbs": round(dec.bytes / (k_ms / 1e3) / 1e9, 1), "kernel_ms": round(k_ms, 4),
+        "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                     "frac": round(alg / (k_ms / 1e3) / 1e9 / hbm, 4)},
+        "bytes_per_launch": alg,
+    }}
+    del dec
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_only(args, rank, world):
     """One secondary workload alone (a short run for a profiling capture)."""
     from paged_kv_cache_303_gb300 import build
     build.build()
     pk, _ = peaks()
     hbm, tfl = float(pk["hbm_gbs"]), float(pk["bf16_tflops"])
-    fn = {"prefill_varlen": lambda: section_prefill_varlen(args, world, hbm, tfl),
+    fn = {"decode": lambda: section_decode(args, world, hbm),
+          "prefill_varlen": lambda: section_prefill_varlen(args, world, hbm, tfl),
           "qk_norm_rope_store": lambda: section_prologue(args, world, hbm),
           "prefill_prefix": lambda: section_prefill_prefix(args, world, tfl),
           "decode_large": lambda: section_decode_large(args, world, hbm)}[args.only]
@@ -757,8 +777,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-large", action="store_true")
-    ap.add_argument("--only", choices=["prefill_varlen", "qk_norm_rope_store", "prefill_prefix",
-                                       "decode_large"], default=None,
+    ap.add_argument("--only", choices=["decode", "prefill_varlen", "qk_norm_rope_store",
+                                       "prefill_prefix", "decode_large"], default=None,
                     help="run one secondary workload alone (for profiling captures)")
     ap.add_argument("--large-batch", type=int, default=256)
     ap.add_argument("--large-pool", type=int, default=40000)

@@ -240,104 +240,6 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
         : "memory");
 }
 
-// ---------------------------------------------------------------------------
-// Pairs of CTAs (a cluster of 2 on two SMs) and the cta_group::2 forms
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// every thread of both CTAs; release / acquire at cluster scope
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// shared::cta address of this CTA -> the same offset in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_try_wait_cl_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void tmem_alloc2(uint32_t *slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
-                 "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish2() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-// D (both CTAs' TMEM, 256 rows) = A (each CTA's 128 rows, shared memory)
-// x B (N split across the pair's shared memory)
-__device__ __forceinline__ void umma2_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// the same with A read from each CTA's tensor memory
-__device__ __forceinline__ void umma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// arrive on the barrier at this offset in both CTAs once the issued MMAs complete
-__device__ __forceinline__ void umma2_commit_both(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"((uint16_t)3)
-        : "memory");
-}
-// arrive on this CTA's barrier only
-__device__ __forceinline__ void umma2_commit_local(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
-}
-// 3-D tiled TMA load into this CTA's shared memory whose completion is
-// signalled on a barrier of either CTA of the pair (a shared::cluster address)
-__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cluster,
-                                                 int x, int y, int z, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster), "l"(policy)
-        : "memory");
-}
-
 // Wait that gives up when another role has aborted, or after the time bound
 // (then it raises the abort flag itself).
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
@@ -345,22 +247,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     const long long t0 = clock64();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
-        if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) {
-            *abort_flag = 1;
-            atomicOr(&g_prefill_status, PKV_STATUS_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-// The same at cluster scope (barriers that the other CTA of a pair arrives
-// on, or that pair MMAs signal).
-__device__ __forceinline__ bool wait_or_abort_cl(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
-    if (mbar_try_wait_cl(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (;;) {
-        if (mbar_try_wait_cl_sleep(bar, parity, kSuspendNs)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitCycles) {
             *abort_flag = 1;
@@ -392,16 +278,13 @@ struct PrefillParams {
     // are copied row by row from the caches instead of by TMA boxes
     int32_t row_copy;
     const uint16_t *k_cache, *v_cache;
-    int32_t rows_per_item;       // 128 (one CTA per item) or 256 (a pair of CTAs)
 };
 
-// key tiles that the query rows [row0, row0 + rows) of a sequence see
-__device__ __forceinline__ int kv_tiles_rows(int Lq, int Lk, int row0, int rows) {
-    const int t_last = min(Lq, row0 + rows) - 1;
+__device__ __forceinline__ int kv_tiles_for(int Lq, int Lk, int mb) {
+    const int t_last = min(Lq, (mb + 1) * kBM) - 1;
     const int keys = Lk - Lq + t_last + 1;
     return (keys + kBN - 1) / kBN;
 }
-__device__ __forceinline__ int kv_tiles_for(int Lq, int Lk, int mb) { return kv_tiles_rows(Lq, Lk, mb * kBM, kBM); }
 
 // Work list: every (sequence, 128-row block), ordered by decreasing number
 // of key tiles (a counting sort on the cost).  One CTA: a warp per sequence,
@@ -416,7 +299,6 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    const int R = p.rows_per_item;
     for (int i = threadIdx.x; i < kCostBins; i += blockDim.x) hist[i] = 0;
     if (threadIdx.x == 0) top = 0;
     __syncthreads();
@@ -428,10 +310,10 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int
             if (lane == 0) atomicOr(&g_prefill_status, PKV_STATUS_BAD_LENGTH);
             continue;
         }
-        const int nmb = (Lq + R - 1) / R;
+        const int nmb = (Lq + kBM - 1) / kBM;
         for (int mb = lane; mb < nmb; mb += 32)
-            atomicAdd(&hist[min(kv_tiles_rows(Lq, Lk, mb * R, R), kCostBins - 1)], 1);
-        if (lane == 0) atomicMax(&top, min(kv_tiles_rows(Lq, Lk, (nmb - 1) * R, R), kCostBins - 1));
+            atomicAdd(&hist[min(kv_tiles_for(Lq, Lk, mb), kCostBins - 1)], 1);
+        if (lane == 0) atomicMax(&top, min(kv_tiles_for(Lq, Lk, nmb - 1), kCostBins - 1));
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -449,9 +331,9 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int
         const int Lq = p.cu_q[s + 1] - p.cu_q[s];
         const int Lk = p.cu_k[s + 1] - p.cu_k[s];
         if (Lq <= 0 || Lk < Lq) continue;
-        const int nmb = (Lq + R - 1) / R;
+        const int nmb = (Lq + kBM - 1) / kBM;
         for (int mb = lane; mb < nmb; mb += 32) {
-            const int pos = atomicAdd(&hist[min(kv_tiles_rows(Lq, Lk, mb * R, R), kCostBins - 1)], 1);
+            const int pos = atomicAdd(&hist[min(kv_tiles_for(Lq, Lk, mb), kCostBins - 1)], 1);
             if (pos < p.max_items) work[pos] = make_int2(s, mb);
         }
     }
@@ -901,498 +783,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     }
 }
 
-// ===========================================================================
-// Pair kernel: a cluster of two CTAs on two SMs runs each product as one
-// cta_group::2 MMA with M = 256 rows.  CTA r of the pair takes query head
-// h0 + r (the two heads share a kv head: the group size is even) over the
-// same 256 query rows of one sequence, as two 128-row blocks b = 0, 1 that
-// ping-pong on the tensor core like the two heads of prefill_kernel.  Every
-// K/V tile is split between the pair: CTA r loads keys 64r .. 64r+63 of each
-// K tile (its half of N for S = Q K^T) and head_dim 64r .. 64r+63 of each V
-// tile (its half of N for O += P V), so each SM's shared memory delivers half
-// of every B operand and receives half of every tile.  That is what the
-// single-CTA kernel runs short of: its S products alone read 128 bytes of
-// shared memory a cycle at full MMA rate, the whole of what an SM delivers.
-//
-// Roles per CTA (320 threads): warps 0-3 softmax of block 0, warps 4-7
-// softmax of block 1 (thread = query row = TMEM lane), warp 8 TMA producer,
-// warp 9 TMEM allocation (both CTAs) and, in the leader (rank 0), the MMA
-// issuer for the pair.  Tensor memory per CTA: S/P of block b at 128 b, O of
-// block b at 256 + 128 b.
-//
-// Synchronisation of the pair (barriers in the leader unless stated):
-//   q_full, slot_full[s]  TMA transaction barriers for both CTAs' halves; the
-//                         leader posts the expected bytes of both halves of a
-//                         load, then lets the peer issue its half (go[s], in
-//                         the peer), so every copy in flight is accounted for
-//                         by a leader barrier the leader drains before exit;
-//   slot_free[s], s_full[b], o_done   MMA commits multicast to both CTAs;
-//   p_full[b]             8 warp arrivals, 4 of them from the peer;
-//   v_fix, vready         paged mode: the value rows past the last key of
-//                         the final tile are zeroed in both CTAs before P V.
-// Both CTAs meet at a cluster barrier after set-up (every barrier exists
-// before anything signals it) and before the tensor memory is released (no
-// CTA leaves while the pair's MMAs or copies still touch it).
-// ===========================================================================
-#ifndef PKV_PF_PAIR
-#define PKV_PF_PAIR 0   // prefill on pairs of SMs where the shapes allow it
-#endif
-constexpr int kPairSlots = 10;            // ring of half tiles
-constexpr int kPairHalf = 16384;          // K half: 64 keys x 128 dims; V half: 128 keys x 64 dims
-constexpr int kPairRows = 2 * kBM;        // query rows per work item
-
-struct PairLayout {
-    static constexpr int kQBlock = 2 * kBM * 128;                 // one 128-row block of Q (32 KB)
-    static constexpr int kOffRing = 2 * kQBlock;
-    static constexpr int kOffBar = kOffRing + kPairSlots * kPairHalf;
-    static constexpr int kBytes = kOffBar + 512;
-};
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-prefill_pair_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-    constexpr int HD = 128;
-    using L = PairLayout;
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
-    uint64_t *q_full = bars;
-    uint64_t *slot_full = q_full + 1;              // [kPairSlots] leader
-    uint64_t *slot_free = slot_full + kPairSlots;  // [kPairSlots] both
-    uint64_t *go = slot_free + kPairSlots;         // [kPairSlots] peer
-    uint64_t *s_full = go + kPairSlots;            // [2] both
-    uint64_t *p_full = s_full + 2;                 // [2] leader, 8 arrivals
-    uint64_t *o_done = p_full + 2;                 // both
-    uint64_t *v_fix = o_done + 1;                  // leader, 2 arrivals
-    uint64_t *vready = v_fix + 1;                  // peer
-    uint64_t *drain = vready + 1;                  // leader
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(drain + 2);
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const uint32_t rank = cluster_rank();
-    const bool leader = rank == 0;
-
-    if (warp == kMmaWarp) {
-        tmem_alloc2(tmem_slot, 512);
-        tmem_relinquish2();
-    }
-    if (tid == 0) {
-        mbar_init(q_full, 1);
-        for (int s = 0; s < kPairSlots; ++s) {
-            mbar_init(&slot_full[s], 1);
-            mbar_init(&slot_free[s], 1);
-            mbar_init(&go[s], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], 8);
-        }
-        mbar_init(o_done, 1);
-        mbar_init(v_fix, 2);
-        mbar_init(vready, 1);
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    if (warp == kProducerWarp && lane == 0) {
-        prefetch_tensormap(&qmap);
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&vmap);
-    }
-#if PKV_PF_PDL
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-#endif
-    const int item = blockIdx.y;
-    const bool idle = item >= p.max_items || item >= *p.work_count;     // uniform for the pair
-    const int2 w = idle ? make_int2(0, 0) : p.work[item];
-    const int seq = w.x, sb = w.y;
-    const int q0 = idle ? 0 : p.cu_q[seq];
-    const int Lq = idle ? 1 : p.cu_q[seq + 1] - q0;
-    const int k0 = idle ? 0 : p.cu_k[seq];
-    const int Lk = idle ? 1 : p.cu_k[seq + 1] - k0;
-    const int off = Lk - Lq;
-    const int r0 = sb * kPairRows;
-    const bool two = Lq - r0 > kBM;               // block 1 holds rows of the sequence
-    const int nkv0 = kv_tiles_rows(Lq, Lk, r0, kBM);
-    const int nkv1 = two ? kv_tiles_rows(Lq, Lk, r0 + kBM, kBM) : 0;
-    const int n_kv = two ? nkv1 : nkv0;           // nkv1 >= nkv0
-    const int G = p.num_heads / p.num_kv_heads;
-    const int h = blockIdx.x;                     // = 2 * pair + rank
-    const int kvh = h / G;
-
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    if (!idle && warp == kProducerWarp) {
-        // ------------------------------------------------------------------
-        // producer: Q blocks, then K_0, V_0, K_1, ... halves (load n -> slot
-        // n % kPairSlots)
-        // ------------------------------------------------------------------
-        const int bs = p.block_size;
-        const int TBK = p.paged ? (bs < 64 ? bs : 64) : 64;
-        const int TBV = p.paged ? (bs < kBN ? bs : kBN) : kBN;
-        const int32_t *bt_row = p.paged ? p.bt + (int64_t)seq * p.bt_stride : nullptr;
-        auto block_of = [&](int pos) -> int {
-            const int lb = pos / bs;
-            const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
-            return (blk >= 0 && blk < p.num_blocks) ? blk : -1;
-        };
-        // loaded segments of a K half (rows 64 r' .. of key tile j) / a V tile
-        auto k_segs = [&](int j, int rr) -> int {
-            int c = 0;
-            for (int sg = 0; sg < 64 / TBK; ++sg) {
-                const int pos = j * kBN + 64 * rr + sg * TBK;
-                if (pos >= Lk) break;
-                if (block_of(pos) >= 0) ++c;
-            }
-            return c;
-        };
-        auto v_segs = [&](int j) -> int {
-            int c = 0;
-            for (int sg = 0; sg < kBN / TBV; ++sg) {
-                const int pos = j * kBN + sg * TBV;
-                if (pos >= Lk) break;
-                if (block_of(pos) >= 0) ++c;
-            }
-            return c;
-        };
-        int issued = 0;
-        bool ok = true;
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            const uint32_t q_bar = map_to_rank(smem_u32(q_full), 0);
-            const int nq = two ? 2 : 1;
-            if (leader) mbar_arrive_expect_tx(q_full, (uint32_t)(2 * nq * L::kQBlock));
-            for (int b = 0; b < nq; ++b)
-                for (int hf = 0; hf < 2; ++hf)
-                    tma_load_3d_pair(smem + b * L::kQBlock + hf * kBM * 128, &qmap, q_bar, hf * 64, h,
-                                     q0 + r0 + b * kBM, pol);
-            for (int n = 0; n < 2 * n_kv; ++n) {
-                const int s = n % kPairSlots;
-                const int j = n >> 1;
-                const bool isv = n & 1;
-                const uint32_t ph = (uint32_t)(n / kPairSlots) & 1u;
-                if (leader) {
-                    if (n >= kPairSlots && !wait_or_abort_cl(&slot_free[s], ph ^ 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    uint32_t bytes;
-                    if (!p.paged)
-                        bytes = 2u * kPairHalf;
-                    else if (isv)
-                        bytes = 2u * (uint32_t)v_segs(j) * TBV * 128u;
-                    else
-                        bytes = (uint32_t)(k_segs(j, 0) + k_segs(j, 1)) * TBK * 256u;
-                    mbar_arrive_expect_tx(&slot_full[s], bytes);
-                    mbar_arrive_cluster(map_to_rank(smem_u32(&go[s]), 1));   // the peer may load its half
-                } else if (!wait_or_abort_cl(&go[s], ph, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t bar = map_to_rank(smem_u32(&slot_full[s]), 0);
-                unsigned char *dst = smem + L::kOffRing + s * kPairHalf;
-                if (!isv) {
-                    // keys 64 rank .. 64 rank + 63 of tile j, all of head_dim
-                    if (!p.paged) {
-                        for (int hf = 0; hf < 2; ++hf)
-                            tma_load_3d_pair(dst + hf * 64 * 128, &kmap, bar, hf * 64, kvh,
-                                             k0 + j * kBN + 64 * (int)rank, pol);
-                    } else {
-                        for (int sg = 0; sg < 64 / TBK; ++sg) {
-                            const int pos = j * kBN + 64 * (int)rank + sg * TBK;
-                            if (pos >= Lk) break;
-                            const int blk = block_of(pos);
-                            if (blk < 0) {
-                                atomicOr(&g_prefill_status, PKV_STATUS_BAD_BLOCK);
-                                continue;
-                            }
-                            const int z = (int)((int64_t)blk * bs + pos % bs);
-                            for (int hf = 0; hf < 2; ++hf)
-                                tma_load_3d_pair(dst + hf * 64 * 128 + sg * TBK * 128, &kmap, bar, hf * 64, kvh,
-                                                 z, pol);
-                        }
-                    }
-                } else {
-                    // all 128 keys of tile j, head_dim 64 rank .. 64 rank + 63
-                    if (!p.paged) {
-                        tma_load_3d_pair(dst, &vmap, bar, 64 * (int)rank, kvh, k0 + j * kBN, pol);
-                    } else {
-                        for (int sg = 0; sg < kBN / TBV; ++sg) {
-                            const int pos = j * kBN + sg * TBV;
-                            if (pos >= Lk) break;
-                            const int blk = block_of(pos);
-                            if (blk < 0) continue;
-                            const int z = (int)((int64_t)blk * bs + pos % bs);
-                            tma_load_3d_pair(dst + sg * TBV * 128, &vmap, bar, 64 * (int)rank, kvh, z, pol);
-                        }
-                    }
-                }
-                ++issued;
-            }
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        // paged: zero the value rows past the last key of the final tile in
-        // both CTAs once it has landed, so unwritten slots never meet a zero
-        // probability
-        if (ok && p.paged && n_kv * kBN > Lk) {
-            const int nv = 2 * n_kv - 1;
-            const int sv = nv % kPairSlots;
-            int landed = 1;
-            if (lane == 0)
-                landed = (leader ? wait_or_abort_cl(&slot_full[sv], (uint32_t)(nv / kPairSlots) & 1u, abort_flag)
-                                 : wait_or_abort_cl(vready, 0, abort_flag)) ? 1 : 0;
-            if (__shfl_sync(0xffffffffu, landed, 0)) {
-                unsigned char *vt = smem + L::kOffRing + sv * kPairHalf;
-                for (int r = Lk - (n_kv - 1) * kBN; r < kBN; ++r)
-                    *reinterpret_cast<uint32_t *>(vt + r * 128 + lane * 4) = 0u;
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (leader) {
-                        mbar_arrive_cluster(map_to_rank(smem_u32(vready), 1));
-                        mbar_arrive(v_fix);
-                    } else {
-                        mbar_arrive_cluster(map_to_rank(smem_u32(v_fix), 0));
-                    }
-                }
-            }
-        }
-        if (lane == 0 && leader) {
-            // no copy of either CTA may still be landing when the pair leaves:
-            // every copy in flight was posted on one of these barriers
-            const long long t0 = clock64();
-            for (int n = issued - kPairSlots < 0 ? 0 : issued - kPairSlots; n < issued; ++n)
-                while (!mbar_try_wait_cl(&slot_full[n % kPairSlots], (uint32_t)(n / kPairSlots) & 1u) &&
-                       clock64() - t0 < kWaitCycles) {
-                }
-            while (!mbar_try_wait_cl(q_full, 0) && clock64() - t0 < kWaitCycles) {
-            }
-        }
-    } else if (!idle && warp == kMmaWarp) {
-        // ------------------------------------------------------------------
-        // MMA issuer of the pair (leader, lane 0).  Order per key tile j:
-        // P_0(j) V_j, S_0(j+1), P_1(j) V_j, S_1(j+1); block b stops after its
-        // own last key tile.
-        // ------------------------------------------------------------------
-        if (leader && lane == 0) {
-            constexpr uint32_t kIdS = idesc_bf16(2 * kBM, kBN, false);
-            constexpr uint32_t kIdO = idesc_bf16(2 * kBM, HD, true);
-            const uint32_t sbase = smem_u32(smem);
-            const uint32_t ring = sbase + L::kOffRing;
-            auto issue_S = [&](int j, int b) {
-                const uint64_t a0 = sdesc_sw128(sbase + b * L::kQBlock, 16, 1024);
-                const uint64_t b0 = sdesc_sw128(ring + ((2 * j) % kPairSlots) * kPairHalf, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t astep = (uint32_t)(((kk / 4) * kBM * 128 + (kk % 4) * 32) >> 4);
-                    const uint32_t bstep = (uint32_t)(((kk / 4) * 64 * 128 + (kk % 4) * 32) >> 4);
-                    umma2_ss(tmem + b * kBN, a0 + astep, b0 + bstep, kIdS, kk > 0 ? 1u : 0u);
-                }
-                umma2_commit_both(&s_full[b]);
-            };
-            auto issue_PV = [&](int j, int b) {
-                const uint64_t b0 = sdesc_sw128(ring + ((2 * j + 1) % kPairSlots) * kPairHalf, kBN * 128, 1024);
-                const uint32_t a_tm = tmem + b * kBN + kColP;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    umma2_ts(tmem + 2 * kBN + b * HD, a_tm + kk * 8, b0 + (uint32_t)((kk * 16 * 128) >> 4), kIdO,
-                             (j > 0 || kk > 0) ? 1u : 0u);
-            };
-            bool live = wait_or_abort_cl(q_full, 0, abort_flag) && wait_or_abort_cl(&slot_full[0], 0, abort_flag);
-            if (live) {
-                tc_fence_after();
-                issue_S(0, 0);
-                if (two) issue_S(0, 1);
-                umma2_commit_both(&slot_free[0]);
-            }
-            for (int j = 0; j < n_kv && live; ++j) {
-                const int nv = 2 * j + 1;
-                const int nk = 2 * j + 2;
-                const bool next = j + 1 < n_kv;
-                live = wait_or_abort_cl(&slot_full[nv % kPairSlots], (uint32_t)(nv / kPairSlots) & 1u, abort_flag);
-                if (live && p.paged && !next && (j + 1) * kBN > Lk) live = wait_or_abort_cl(v_fix, 0, abort_flag);
-                if (live && next)
-                    live = wait_or_abort_cl(&slot_full[nk % kPairSlots], (uint32_t)(nk / kPairSlots) & 1u,
-                                            abort_flag);
-                for (int b = 0; b < 2 && live; ++b) {
-                    const int nb = b == 0 ? nkv0 : nkv1;
-                    if (j >= nb) continue;
-                    live = wait_or_abort_cl(&p_full[b], (uint32_t)j & 1u, abort_flag);
-                    if (!live) break;
-                    tc_fence_after();
-                    issue_PV(j, b);
-                    if (j + 1 < nb) issue_S(j + 1, b);
-                }
-                if (live) {
-                    umma2_commit_both(&slot_free[nv % kPairSlots]);                // V_j
-                    if (next) umma2_commit_both(&slot_free[nk % kPairSlots]);      // K_{j+1}
-                }
-            }
-            if (live) umma2_commit_both(o_done);
-            // every MMA of the pair has completed before the pair leaves
-            umma2_commit_local(drain);
-            (void)mbar_wait(drain, 0);
-        }
-        __syncwarp();
-    } else if (!idle && warp < 8) {
-        // ------------------------------------------------------------------
-        // softmax warpgroups: block b = warp / 4, thread = query row = TMEM lane
-        // ------------------------------------------------------------------
-        const int b = warp >> 2;
-        if (b == 0 || two) {
-            const int nb = b == 0 ? nkv0 : nkv1;
-            const int row = tid & (kBM - 1);
-            const int qi = r0 + b * kBM + row;          // query index within the sequence
-            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-            const uint32_t tS = tmem + lane_base + b * kBN;
-            const uint32_t tO = tmem + lane_base + 2 * kBN + b * HD;
-            const uint32_t p_bar = leader ? smem_u32(&p_full[b]) : map_to_rank(smem_u32(&p_full[b]), 0);
-            const float sc = p.scale_log2;
-            float m = -INFINITY, l = 0.f;
-            bool live = true;
-            for (int j = 0; j < nb; ++j) {
-                live = wait_or_abort_cl(&s_full[b], (uint32_t)j & 1u, abort_flag);
-                if (!__all_sync(0xffffffffu, live)) { live = false; break; }
-                tc_fence_after();
-                const int limit = off + qi - j * kBN;   // columns <= limit are visible
-                uint32_t sr[kBN];
-                tmem_ld128(tS, sr);
-                if (limit < kBN - 1) {
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c)
-                        if (c > limit) sr[c] = __float_as_uint(-INFINITY);
-                }
-                float pm[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    pm[i] = fmaxf(__uint_as_float(sr[i]), __uint_as_float(sr[4 + i]));
-#pragma unroll
-                for (int c = 8; c < kBN; c += 8)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        pm[i] = fmax3(pm[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 4 + i]));
-                const float rmax = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
-                const float m_new = fmaxf(m, rmax * sc);
-                const bool rescale = (m == -INFINITY) ? (m_new != -INFINITY)
-                                                      : (m_new > m + kRescaleThreshold);
-                float alpha = 1.f;
-                if (rescale) {
-                    alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - m_new);
-                    m = m_new;
-                }
-                const float mu = (m == -INFINITY) ? 0.f : m;
-                const bool any_rescale = __any_sync(0xffffffffu, rescale);
-                float2 acc[2];
-                exp_pack_store(sr, sc, mu, tS, acc);
-                // S_b(j) follows P_b(j-1) V_{j-1} on the tensor core, so O is
-                // final for the earlier tiles: rescale it in place if needed
-                if (j > 0 && any_rescale) {
-#pragma unroll 1
-                    for (int cc = 0; cc < HD / 32; ++cc) {
-                        float o[32];
-                        tmem_ld32(tO + cc * 32, o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(tO + cc * 32, o);
-                    }
-                }
-                l *= alpha;
-                tmem_wait_st();
-                l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(p_bar);
-            }
-            // epilogue: O / l -> bf16 rows of head h, lse
-            if (live) live = wait_or_abort_cl(o_done, 0, abort_flag);
-            if (__all_sync(0xffffffffu, live)) {
-                tc_fence_after();
-                const bool row_ok = qi < Lq;
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                uint16_t *orow = p.out + (int64_t)(q0 + (row_ok ? qi : 0)) * p.out_rs + (int64_t)h * HD;
-#pragma unroll
-                for (int cc = 0; cc < HD / 32; ++cc) {
-                    float o[32];
-                    tmem_ld32(tO + cc * 32, o);
-                    if (row_ok) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 pkt;
-                            pkt.x = pack_bf16x2(o[v * 8 + 0] * inv, o[v * 8 + 1] * inv);
-                            pkt.y = pack_bf16x2(o[v * 8 + 2] * inv, o[v * 8 + 3] * inv);
-                            pkt.z = pack_bf16x2(o[v * 8 + 4] * inv, o[v * 8 + 5] * inv);
-                            pkt.w = pack_bf16x2(o[v * 8 + 6] * inv, o[v * 8 + 7] * inv);
-                            st_cs_v4(orow + cc * 32 + v * 8, pkt);
-                        }
-                    }
-                }
-                if (row_ok && p.lse)
-                    p.lse[(int64_t)(q0 + qi) * p.num_heads + h] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-            }
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();
-    if (warp == kMmaWarp) {
-        tc_fence_after();
-        tmem_dealloc2(tmem, 512);
-    }
-}
-
-// the pair kernel: K halves of 64 keys and V halves of 64 head_dim columns
-int launch_pair(const PrefillArgs &a, const PrefillParams &pp, const CUtensorMap &qm, int max_items,
-                cudaStream_t stream, const char **err) {
-    constexpr int HD = 128;
-    CUtensorMap km, vm;
-    int rc;
-    if (pp.paged) {
-        const int64_t slots = a.num_blocks * a.block_size;
-        const int tbk = a.block_size < 64 ? a.block_size : 64;
-        const int tbv = a.block_size < kBN ? a.block_size : kBN;
-        const int64_t D = (int64_t)a.num_kv_heads * HD;
-        rc = encode_rows_heads_map(&km, a.k_cache, slots, a.num_kv_heads, HD, D, HD, 64, tbk, true, err);
-        if (!rc) rc = encode_rows_heads_map(&vm, a.v_cache, slots, a.num_kv_heads, HD, D, HD, 64, tbv, true, err);
-    } else {
-        rc = encode_rows_heads_map(&km, a.k, a.total_k, a.num_kv_heads, HD, a.k_rs, HD, 64, 64, true, err);
-        if (!rc) rc = encode_rows_heads_map(&vm, a.v, a.total_k, a.num_kv_heads, HD, a.v_rs, HD, 64, kBN, true, err);
-    }
-    if (rc) return rc;
-    const int smem = PairLayout::kBytes + 1024;
-    static PerDeviceOnce once;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess)
-        e = once.run(dev, [&]() {
-            return cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        });
-    if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.num_heads, max_items);        // clusters of 2 along x
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = PKV_PF_PDL ? 1 : 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel, qm, km, vm, pp);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
-    return PKV_OK;
-}
-
 template <int HD>
 int launch_hd(const PrefillArgs &a, const PrefillParams &pp, int2 *work, int32_t *count,
               int max_items, cudaStream_t stream, const char **err) {
@@ -1414,7 +804,6 @@ int launch_hd(const PrefillArgs &a, const PrefillParams &pp, int2 *work, int32_t
     prefill_plan_kernel<<<1, 1024, 0, stream>>>(pp, count, work);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
-    if (pp.rows_per_item == kPairRows) return launch_pair(a, pp, qm, max_items, stream, err);
     const int smem = L::kBytes + 1024;
     auto kern = prefill_kernel<HD>;
     static PerDeviceOnce once;
@@ -1500,14 +889,8 @@ int launch_prefill(const PrefillArgs &a, cudaStream_t stream, const char **err) 
     pp.row_copy = paged && a.block_size < 8 ? 1 : 0;
     pp.k_cache = a.k_cache;
     pp.v_cache = a.v_cache;
-    // pairs of SMs when the two heads of a pair share a kv head, head_dim is
-    // 128 and the caches can be read by TMA boxes
-    const bool pair = PKV_PF_PAIR && a.head_dim == 128 && (a.num_heads / a.num_kv_heads) % 2 == 0 && !pp.row_copy;
-    pp.rows_per_item = pair ? kPairRows : kBM;
-    const int items = pair ? a.num_seqs + (a.total_q + kPairRows - 1) / kPairRows : max_items;
-    pp.max_items = items;
-    if (a.head_dim == 128) return launch_hd<128>(a, pp, work, count, items, stream, err);
-    return launch_hd<64>(a, pp, work, count, items, stream, err);
+    if (a.head_dim == 128) return launch_hd<128>(a, pp, work, count, max_items, stream, err);
+    return launch_hd<64>(a, pp, work, count, max_items, stream, err);
 }
 
 }  // namespace pkv

@@ -771,10 +771,12 @@ std::atomic<int> g_decode_chunk_tiles{0};
 void decode_plan(int32_t batch, int32_t num_kv_heads, int32_t head_dim, int32_t max_context_len,
                  int32_t *chunk, int32_t *max_splits) {
     (void)head_dim;
-    // about three waves of resident CTAs, assuming contexts average half of
-    // the maximum; chunks of 256 .. 2048 keys
+    // about one and a half waves of resident CTAs, assuming contexts average
+    // half of the maximum; chunks of 256 .. 2048 keys.  (Chunks per sweep on
+    // qwen3-decode-b64, step GB/s: 288 keys 6.13, 384 6.26, 512 6.36, 768
+    // 6.28; the group-4 large decode is best at the 2048-key cap.)
     const int64_t keys = (int64_t)batch * num_kv_heads * max_context_len / 2;
-    const int64_t target = (int64_t)num_sms() * PKV_DEC_MIN_CTAS * 3;
+    const int64_t target = (int64_t)num_sms() * PKV_DEC_MIN_CTAS * 3 / 2;
     int64_t per = (keys + target * kTile - 1) / (target * kTile);
     if (per < 8) per = 8;
     if (per > 64) per = 64;

@@ -6,8 +6,8 @@ caller workspace.
 
 The test calls the entry point directly through the C ABI, twice in a row on
 different inputs, and compares each result with the regular
-paged_attn_decode (caller workspace) within the tolerance the other decode
-tests use.  It also checks that a launch needing more scratch than the array
+paged_attn_decode (caller workspace) and with the CPU oracle, within the
+tolerance the other decode tests use.  It also checks that a launch needing more scratch than the array
 holds is refused with PKV_ERR_WORKSPACE before anything runs.
 
 This file is named so that pytest collects it last.
@@ -18,8 +18,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_cache_303_gb300 import ops
 from paged_kv_cache_303_gb300 import workloads as W
+from _util import bits
 
 pytestmark = pytest.mark.gpu
 
@@ -37,9 +39,9 @@ def _noalloc(q, kc, vc, bt, ctx, max_ctx, scale, out, lse):
     return rc, lib.pkv_last_error().decode()
 
 
-def _close(got: torch.Tensor, ref: torch.Tensor):
+def _close(got: torch.Tensor, ref):
     g = got.double().cpu().numpy()
-    r = ref.double().cpu().numpy()
+    r = ref.double().cpu().numpy() if isinstance(ref, torch.Tensor) else np.asarray(ref, np.float64)
     bad = ~(np.abs(g - r) <= TOL + TOL * np.abs(r))
     assert not bad.any(), f"{int(bad.sum())} elements outside tolerance"
 
@@ -73,6 +75,8 @@ def test_noalloc_matches_workspace_decode_twice():
         torch.cuda.synchronize()
         assert rc == 0, msg
         _close(out, ref)
+        oref, _ = oracle.decode(bits(work.q), bits(kc), bits(vc), work.block_tables, ctx, h.scale)
+        _close(out, oref)
         fin = torch.isfinite(ref_lse)
         assert torch.equal(torch.isfinite(lse), fin)
         _close(lse[fin], ref_lse[fin])

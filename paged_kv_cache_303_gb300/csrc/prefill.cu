@@ -86,6 +86,9 @@ constexpr int kCostBins = 2048;
 constexpr int kColP = kBN / 2;
 #ifndef PKV_PF_PDL
 #define PKV_PF_PDL 1   // prefill kernel launched as a programmatic dependent of the planning kernel
+#endif
+#ifndef PKV_PF_PACK
+#define PKV_PF_PACK 1   // blocks of at most 64 rows carry both heads of a pair in one tile
 #endif    // P (bf16 pairs) over the upper half of a head's S columns
 
 // ---------------------------------------------------------------------------
@@ -195,6 +198,26 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
         : "memory");
 }
 
+// 64 consecutive TMEM columns of this warp's lanes -> 64 registers (waits)
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+}
+
+// a row's HD output columns in one go (one wait instead of one per 32)
+template <int HD>
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[HD]) {
+    if constexpr (HD == 128) {
+        tmem_ld128(taddr, r);
+    } else {
+        tmem_ld64(taddr, r);
+    }
+}
+
 // 32 registers -> 32 consecutive TMEM columns of this warp's lanes (no wait)
 __device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t (&v)[32]) {
     asm volatile(
@@ -272,7 +295,9 @@ struct PrefillParams {
     int64_t out_rs;
     float *lse;
     const int32_t *work_count;   // [1]
-    const int2 *work;            // [max_items] (sequence, 128-row block)
+    // [max_items][2]: {sequence, 128-row block, first query row, query rows},
+    // {first key row, keys, key tiles, 0} -- everything a CTA needs to start
+    const int4 *work;
     int32_t max_items;
     // paged mode with blocks shorter than the 8-row swizzle atom: K/V tiles
     // are copied row by row from the caches instead of by TMA boxes
@@ -290,7 +315,7 @@ __device__ __forceinline__ int kv_tiles_for(int Lq, int Lk, int mb) {
 // of key tiles (a counting sort on the cost).  One CTA: a warp per sequence,
 // lanes over its row blocks; the scan runs over the bins in use only.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int32_t *work_count,
-                                                            int2 *work) {
+                                                            int4 *work) {
     __shared__ int hist[kCostBins];
     __shared__ int top;                         // highest cost bin in use
 #if PKV_PF_PDL
@@ -299,12 +324,21 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    // the lengths of this warp's first sequence, kept for the second pass
+    const int s_first = warp < p.num_seqs ? warp : -1;
+    int f_q0 = 0, f_q1 = 0, f_k0 = 0, f_k1 = 0;
+    if (s_first >= 0) {
+        f_q0 = p.cu_q[s_first];
+        f_q1 = p.cu_q[s_first + 1];
+        f_k0 = p.cu_k[s_first];
+        f_k1 = p.cu_k[s_first + 1];
+    }
     for (int i = threadIdx.x; i < kCostBins; i += blockDim.x) hist[i] = 0;
     if (threadIdx.x == 0) top = 0;
     __syncthreads();
     for (int s = warp; s < p.num_seqs; s += nwarps) {
-        const int Lq = p.cu_q[s + 1] - p.cu_q[s];
-        const int Lk = p.cu_k[s + 1] - p.cu_k[s];
+        const int Lq = s == s_first ? f_q1 - f_q0 : p.cu_q[s + 1] - p.cu_q[s];
+        const int Lk = s == s_first ? f_k1 - f_k0 : p.cu_k[s + 1] - p.cu_k[s];
         if (Lq <= 0) continue;
         if (Lk < Lq) {
             if (lane == 0) atomicOr(&g_prefill_status, PKV_STATUS_BAD_LENGTH);
@@ -328,13 +362,19 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int
     }
     __syncthreads();
     for (int s = warp; s < p.num_seqs; s += nwarps) {
-        const int Lq = p.cu_q[s + 1] - p.cu_q[s];
-        const int Lk = p.cu_k[s + 1] - p.cu_k[s];
+        const int q0 = s == s_first ? f_q0 : p.cu_q[s];
+        const int k0 = s == s_first ? f_k0 : p.cu_k[s];
+        const int Lq = (s == s_first ? f_q1 : p.cu_q[s + 1]) - q0;
+        const int Lk = (s == s_first ? f_k1 : p.cu_k[s + 1]) - k0;
         if (Lq <= 0 || Lk < Lq) continue;
         const int nmb = (Lq + kBM - 1) / kBM;
         for (int mb = lane; mb < nmb; mb += 32) {
-            const int pos = atomicAdd(&hist[min(kv_tiles_for(Lq, Lk, mb), kCostBins - 1)], 1);
-            if (pos < p.max_items) work[pos] = make_int2(s, mb);
+            const int nkv = kv_tiles_for(Lq, Lk, mb);
+            const int pos = atomicAdd(&hist[min(nkv, kCostBins - 1)], 1);
+            if (pos < p.max_items) {
+                work[2 * pos] = make_int4(s, mb, q0, Lq);
+                work[2 * pos + 1] = make_int4(k0, Lk, nkv, 0);
+            }
         }
     }
 }
@@ -355,8 +395,9 @@ struct PLayout {
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-               const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap qmap64,
+               const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+               const PrefillParams p) {
     using L = PLayout<HD>;
     constexpr int H = L::H;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -401,6 +442,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     }
     if (warp == kProducerWarp && lane == 0) {
         prefetch_tensormap(&qmap);
+        prefetch_tensormap(&qmap64);
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
     }
@@ -408,21 +450,51 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // the work list is written by the planning kernel launched just before
     asm volatile("griddepcontrol.wait;" ::: "memory");
 #endif
+    // the item's record and the item count are read together (one memory
+    // round trip); a record past the count is not used
     const int item = blockIdx.y;
-    const bool idle = item >= p.max_items || item >= *p.work_count;     // uniform for the CTA
-    const int2 w = idle ? make_int2(0, 0) : p.work[item];
-    const int seq = w.x, mb = w.y;
-    const int q0 = idle ? 0 : p.cu_q[seq];
-    const int Lq = idle ? 1 : p.cu_q[seq + 1] - q0;
-    const int k0 = idle ? 0 : p.cu_k[seq];
-    const int Lk = idle ? 1 : p.cu_k[seq + 1] - k0;
+    const bool in_range = item < p.max_items;
+    int4 w0 = make_int4(0, 0, 0, 1), w1 = make_int4(0, 1, 1, 0);
+    if (in_range) {
+        w0 = p.work[2 * item];
+        w1 = p.work[2 * item + 1];
+    }
+    const bool idle = !in_range || item >= *p.work_count;              // uniform for the CTA
+    if (idle) {
+        w0 = make_int4(0, 0, 0, 1);
+        w1 = make_int4(0, 1, 1, 0);
+    }
+    const int seq = w0.x, mb = w0.y;
+    const int q0 = w0.z, Lq = w0.w;
+    const int k0 = w1.x, Lk = w1.y;
     const int off = Lk - Lq;
     const int r0 = mb * kBM;
-    const int n_kv = kv_tiles_for(Lq, Lk, mb);
+    const int n_kv = w1.z;
     const int G = p.num_heads / p.num_kv_heads;
-    const int ntile = G % 2 == 0 ? 2 : 1;        // two heads of one group, or one head
-    const int h0 = blockIdx.x * ntile;
+    const int pair = G % 2 == 0 ? 2 : 1;         // two heads of one group, or one head
+    const int h0 = blockIdx.x * pair;
     const int kvh = h0 / G;
+    // A block with at most 64 query rows (the last block of a sequence, or a
+    // short one) holds both heads in one 128-row tile: head h0 in rows 0..63,
+    // head h0+1 in rows 64..127.  The two heads share every K/V tile, so one
+    // S and one P V stream cover both and the half-empty rows are not computed
+    // twice.
+    const bool packed = PKV_PF_PACK && pair == 2 && Lq - r0 <= kBM / 2;
+    const int ntile = packed ? 1 : pair;
+    auto load_q = [&](uint64_t pol) {
+        mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * L::kQTile));
+        if (packed) {
+            for (int t = 0; t < 2; ++t)
+                for (int hf = 0; hf < H; ++hf)
+                    tma_load_3d(smem + hf * kBM * 128 + t * (kBM / 2) * 128, &qmap64, q_full, hf * 64,
+                                h0 + t, q0 + r0, pol);
+        } else {
+            for (int t = 0; t < ntile; ++t)
+                for (int hf = 0; hf < H; ++hf)
+                    tma_load_3d(smem + t * L::kQTile + hf * kBM * 128, &qmap, q_full, hf * 64, h0 + t,
+                                q0 + r0, pol);
+        }
+    };
 
     tc_fence_before();
     __syncthreads();
@@ -445,14 +517,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // every lane waits for its own pieces, fences them into the async
         // proxy that the tensor core reads through, then lane 0 arrives.
         // ------------------------------------------------------------------
-        if (lane == 0) {
-            const uint64_t pol_stream = policy_evict_first();
-            mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * L::kQTile));
-            for (int t = 0; t < ntile; ++t)
-                for (int hf = 0; hf < H; ++hf)
-                    tma_load_3d(smem + t * L::kQTile + hf * kBM * 128, &qmap, q_full, hf * 64, h0 + t,
-                                q0 + r0, pol_stream);
-        }
+        if (lane == 0) load_q(policy_evict_first());
         constexpr int CPR = HD / 8;                  // 16-byte pieces per row
         const int bs = p.block_size;
         const int32_t *bt_row = p.bt + (int64_t)seq * p.bt_stride;
@@ -520,11 +585,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         int issued_n = 0;
         if (lane == 0) {
             const uint64_t pol_stream = policy_evict_first();
-            mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * L::kQTile));
-            for (int t = 0; t < ntile; ++t)
-                for (int hf = 0; hf < H; ++hf)
-                    tma_load_3d(smem + t * L::kQTile + hf * kBM * 128, &qmap, q_full, hf * 64, h0 + t,
-                                q0 + r0, pol_stream);
+            load_q(pol_stream);
             const int bs = p.block_size;
             const int TB = p.paged ? (bs < kBN ? bs : kBN) : kBN;
             const int32_t *bt_row = p.paged ? p.bt + (int64_t)seq * p.bt_stride : nullptr;
@@ -677,7 +738,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         const int t = warp >> 2;
         if (t < ntile) {
             const int row = tid & (kBM - 1);
-            const int qi = r0 + row;                    // query index within the sequence
+            // query index within the sequence (packed: rows 64.. are head h0+1)
+            const int qi = r0 + (packed ? (row & (kBM / 2 - 1)) : row);
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
             const uint32_t tS = tmem + lane_base + L::kColS + t * kBN;
             const uint32_t tO = tmem + lane_base + L::kColO + t * HD;
@@ -750,22 +812,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 tc_fence_after();
                 const bool row_ok = qi < Lq;
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                const int hq = h0 + t;
+                const int hq = packed ? h0 + (row >> 6) : h0 + t;
                 uint16_t *orow = p.out + (int64_t)(q0 + (row_ok ? qi : 0)) * p.out_rs + (int64_t)hq * HD;
+                uint32_t ov[HD];
+                tmem_ld_row<HD>(tO, ov);
+                if (row_ok) {
 #pragma unroll
-                for (int cc = 0; cc < HD / 32; ++cc) {
-                    float o[32];
-                    tmem_ld32(tO + cc * 32, o);
-                    if (row_ok) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 pkt;
-                            pkt.x = pack_bf16x2(o[v * 8 + 0] * inv, o[v * 8 + 1] * inv);
-                            pkt.y = pack_bf16x2(o[v * 8 + 2] * inv, o[v * 8 + 3] * inv);
-                            pkt.z = pack_bf16x2(o[v * 8 + 4] * inv, o[v * 8 + 5] * inv);
-                            pkt.w = pack_bf16x2(o[v * 8 + 6] * inv, o[v * 8 + 7] * inv);
-                            st_cs_v4(orow + cc * 32 + v * 8, pkt);   // written once
-                        }
+                    for (int v = 0; v < HD / 8; ++v) {
+                        uint4 pkt;
+                        pkt.x = pack_bf16x2(__uint_as_float(ov[v * 8 + 0]) * inv, __uint_as_float(ov[v * 8 + 1]) * inv);
+                        pkt.y = pack_bf16x2(__uint_as_float(ov[v * 8 + 2]) * inv, __uint_as_float(ov[v * 8 + 3]) * inv);
+                        pkt.z = pack_bf16x2(__uint_as_float(ov[v * 8 + 4]) * inv, __uint_as_float(ov[v * 8 + 5]) * inv);
+                        pkt.w = pack_bf16x2(__uint_as_float(ov[v * 8 + 6]) * inv, __uint_as_float(ov[v * 8 + 7]) * inv);
+                        st_cs_v4(orow + v * 8, pkt);   // written once
                     }
                 }
                 if (row_ok && p.lse)
@@ -784,11 +843,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 }
 
 template <int HD>
-int launch_hd(const PrefillArgs &a, const PrefillParams &pp, int2 *work, int32_t *count,
+int launch_hd(const PrefillArgs &a, const PrefillParams &pp, int4 *work, int32_t *count,
               int max_items, cudaStream_t stream, const char **err) {
     using L = PLayout<HD>;
-    CUtensorMap qm, km, vm;
+    CUtensorMap qm, qm64, km, vm;
     int rc = encode_rows_heads_map(&qm, a.q, a.total_q, a.num_heads, HD, a.q_rs, HD, 64, kBM, true, err);
+    if (!rc) rc = encode_rows_heads_map(&qm64, a.q, a.total_q, a.num_heads, HD, a.q_rs, HD, 64, kBM / 2, true, err);
     if (rc) return rc;
     if (pp.paged) {
         const int64_t slots = a.num_blocks * a.block_size;
@@ -815,9 +875,9 @@ int launch_hd(const PrefillArgs &a, const PrefillParams &pp, int2 *work, int32_t
         });
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
     const int G = a.num_heads / a.num_kv_heads;
-    const int ntile = G % 2 == 0 ? 2 : 1;
+    const int pair = G % 2 == 0 ? 2 : 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.num_heads / ntile, max_items);
+    cfg.gridDim = dim3(a.num_heads / pair, max_items);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -826,7 +886,7 @@ int launch_hd(const PrefillArgs &a, const PrefillParams &pp, int2 *work, int32_t
     attr[0].val.programmaticStreamSerializationAllowed = PKV_PF_PDL ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, qm, km, vm, pp);
+    e = cudaLaunchKernelEx(&cfg, kern, qm, qm64, km, vm, pp);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
     return PKV_OK;
@@ -842,7 +902,7 @@ size_t prefill_workspace_bytes(int32_t num_seqs, int32_t total_q, int32_t max_se
                                int32_t num_heads) {
     (void)max_seqlen_q;
     (void)num_heads;
-    return 256 + sizeof(int2) * (size_t)max_work_items(num_seqs, total_q);
+    return 256 + 2 * sizeof(int4) * (size_t)max_work_items(num_seqs, total_q);
 }
 
 int launch_prefill(const PrefillArgs &a, cudaStream_t stream, const char **err) {
@@ -866,7 +926,7 @@ int launch_prefill(const PrefillArgs &a, cudaStream_t stream, const char **err) 
         return PKV_ERR_UNSUPPORTED;
     }
     int32_t *count = reinterpret_cast<int32_t *>(a.workspace);
-    int2 *work = reinterpret_cast<int2 *>(reinterpret_cast<unsigned char *>(a.workspace) + 256);
+    int4 *work = reinterpret_cast<int4 *>(reinterpret_cast<unsigned char *>(a.workspace) + 256);
     PrefillParams pp{};
     pp.cu_q = a.cu_q;
     pp.cu_k = a.cu_k;

@@ -170,6 +170,71 @@ __device__ __forceinline__ uint32_t chunk_off(int row, int chunk) {
     return row * 128 + ((SW ? (chunk ^ (row & 7)) : chunk) << 4);
 }
 
+// Merge the chunks of one (sequence, query head) with one warp:
+//   m = max_s m_s, l = sum_s 2^(m_s - m) l_s, o = sum_s 2^(m_s - m) o_s / l
+// The lanes read the (m, l) pairs of 32 chunks at once and the partial
+// outputs eight chunks at a time (independent loads in flight), each chunk's
+// factor passed by shuffle from the lane that computed it.  The partials are
+// read through L2 only (they were written by other SMs and are read once).
+template <int HD>
+__device__ __forceinline__ void merge_head(const DecodeParams &p, int b, int hq, int ns, int lane) {
+    constexpr int EPL = HD / 32;                     // elements per lane
+    constexpr int kAhead = 8;
+    const int64_t part0 = ((int64_t)b * p.num_heads + hq) * p.max_splits;
+    const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml) + part0;
+    float2 ml0 = lane < ns ? __ldcg(ml + lane) : make_float2(-INFINITY, 0.f);
+    float m = ml0.x;
+    for (int s = lane + 32; s < ns; s += 32) m = fmaxf(m, __ldcg(ml + s).x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const float mu = (m == -INFINITY) ? 0.f : m;
+    float l = 0.f;
+    float o[EPL];
+#pragma unroll
+    for (int k = 0; k < EPL; ++k) o[k] = 0.f;
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+        const int cnt = ns - s0 < 32 ? ns - s0 : 32;          // warp-uniform
+        float f = 0.f;
+        if (lane < cnt) {
+            const float2 v = s0 == 0 ? ml0 : __ldcg(ml + s0 + lane);
+            f = fast_exp2(v.x - mu);
+            l += f * v.y;
+        }
+        for (int t = 0; t < cnt; t += kAhead) {
+            float fs[kAhead];
+            float src[kAhead][EPL];
+#pragma unroll
+            for (int u = 0; u < kAhead; ++u) {
+                fs[u] = __shfl_sync(0xffffffffu, f, (t + u) & 31);
+                if (t + u < cnt) {
+                    const float *ps = p.part_o + (part0 + s0 + t + u) * HD + lane * EPL;
+#pragma unroll
+                    for (int k = 0; k < EPL; ++k) src[u][k] = __ldcg(ps + k);
+                } else {
+                    fs[u] = 0.f;
+#pragma unroll
+                    for (int k = 0; k < EPL; ++k) src[u][k] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kAhead; ++u)
+#pragma unroll
+                for (int k = 0; k < EPL; ++k) o[k] += fs[u] * src[u][k];
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    uint16_t *orow = p.out + (int64_t)b * p.out_rs + (int64_t)hq * HD + lane * EPL;
+#pragma unroll
+    for (int k = 0; k < EPL; k += 2) {
+        const uint32_t w = pack_bf16x2(o[k] * inv, o[k + 1] * inv);
+        *reinterpret_cast<uint32_t *>(orow + k) = w;
+    }
+    if (p.lse && lane == 0)
+        p.lse[(int64_t)b * p.num_heads + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+}
+
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
 }
@@ -229,8 +294,7 @@ __global__ void __launch_bounds__(kThreads, PKV_DEC_MIN_CTAS)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
     using L = Layout<HD, G>;
-    constexpr int DPL = HD / 32;                    // head_dim elements per lane in P.V
-    constexpr int CPR = HD / 8;                     // 16-byte chunks per K row
+    constexpr int DPL = HD / 32;                    // head_dim elements per lane of the fused store
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem =
@@ -681,74 +745,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 }
 
 // Merge the chunks of each (sequence, head): one warp per pair.
-//   m = max_s m_s, l = sum_s 2^(m_s - m) l_s, o = sum_s 2^(m_s - m) o_s / l
-// The lanes read the (m, l) pairs of 32 chunks at once, and the partial
-// outputs four chunks at a time (independent loads in flight), each chunk's
-// factor passed by shuffle from the lane that computed it: a few memory
-// round trips per pair instead of two per chunk.
 template <int HD>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
-    constexpr int EPL = HD / 32;                     // elements per lane
-    constexpr int kAhead = 4;                        // chunks' partial outputs in flight
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hq = blockIdx.x * 4 + warp;
     const int b = blockIdx.y;
     if (hq >= p.num_heads) return;
     int ctx = p.ctx[b];
     ctx = ctx < 0 ? 0 : (ctx > p.max_context_len ? p.max_context_len : ctx);
-    const int ns = (ctx + p.chunk - 1) / p.chunk;
-    uint16_t *orow = p.out + (int64_t)b * p.out_rs + (int64_t)hq * HD + lane * EPL;
-    const int64_t part0 = ((int64_t)b * p.num_heads + hq) * p.max_splits;
-    const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml) + part0;
-    float m = -INFINITY;
-    for (int s = lane; s < ns; s += 32) m = fmaxf(m, ml[s].x);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    const float mu = (m == -INFINITY) ? 0.f : m;
-    float l = 0.f;
-    float o[EPL];
-#pragma unroll
-    for (int k = 0; k < EPL; ++k) o[k] = 0.f;
-    for (int s0 = 0; s0 < ns; s0 += 32) {
-        const int cnt = ns - s0 < 32 ? ns - s0 : 32;          // warp-uniform
-        float f = 0.f;
-        if (lane < cnt) {
-            const float2 v = ml[s0 + lane];
-            f = fast_exp2(v.x - mu);
-            l += f * v.y;
-        }
-        for (int t = 0; t < cnt; t += kAhead) {
-            float fs[kAhead];
-            float src[kAhead][EPL];
-#pragma unroll
-            for (int u = 0; u < kAhead; ++u) {
-                fs[u] = __shfl_sync(0xffffffffu, f, (t + u) & 31);
-                if (t + u < cnt) {
-                    const float *ps = p.part_o + (part0 + s0 + t + u) * HD + lane * EPL;
-#pragma unroll
-                    for (int k = 0; k < EPL; ++k) src[u][k] = ps[k];
-                } else {
-                    fs[u] = 0.f;
-#pragma unroll
-                    for (int k = 0; k < EPL; ++k) src[u][k] = 0.f;
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kAhead; ++u)
-#pragma unroll
-                for (int k = 0; k < EPL; ++k) o[k] += fs[u] * src[u][k];
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-    for (int k = 0; k < EPL; k += 2) {
-        const uint32_t w = pack_bf16x2(o[k] * inv, o[k + 1] * inv);
-        *reinterpret_cast<uint32_t *>(orow + k) = w;
-    }
-    if (p.lse && lane == 0)
-        p.lse[(int64_t)b * p.num_heads + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    merge_head<HD>(p, b, hq, (ctx + p.chunk - 1) / p.chunk, lane);
 }
 
 template <int HD, int G, bool SW>

@@ -16,7 +16,8 @@
 //     by 3-D TMA over the cache viewed as [num_slots, num_kv_heads, head_dim]
 //     (box: 64 head_dim elements x 1 head x min(block_size, 32) slots).  With
 //     block_size >= 8 the boxes use the 128-byte swizzle so that the
-//     row-per-lane reads below are bank-conflict free.
+//     ldmatrix fragment reads below (8 rows of 16 bytes each) are
+//     bank-conflict free.
 //   * One producer warp claims items, writes each item's record and query
 //     vectors into a two-entry item queue, and keeps a 2-stage tile ring
 //     full (an mbarrier pair per stage) across item boundaries, so the next
@@ -27,8 +28,8 @@
 //   * Scores and P.V are warp-wide tensor-core products (mma.sync, bf16
 //     inputs, fp32 accumulators): S = q K^T with the group's heads as rows,
 //     then O^T += V^T P^T with the probabilities kept in the registers the
-//     scores came out in.  Scores carry scale*log2(e) so the softmax uses
-//     exp2.  (The two products are small -- G heads by 32 tokens -- and the
+//     scores came out in.  The fp32 scores are multiplied by
+//     scale*log2(e) so the softmax uses exp2.  (The two products are small -- G heads by 32 tokens -- and the
 //     kernel stays HBM-bound; the tensor cores take the instruction count per
 //     tile from about 1800 to about 200, which is what limited it.)
 //   * Softmax: per warp and head, the tile maximum (shuffles) updates the

@@ -9,6 +9,9 @@
 // one GQA group).  The two heads share every K/V tile the CTA loads, which
 // halves K/V traffic per FLOP compared with one head per CTA.  When the
 // group size is odd a CTA takes one head (the second softmax warpgroup idles).
+// A block of at most 64 rows (a sequence's last block, or a short sequence)
+// carries both heads in one 128-row tile, 64 rows each, so its half-empty
+// rows are not computed twice.
 //
 // Roles (320 threads):
 //   warps 0-3  softmax warpgroup of query head A, thread = query row = TMEM lane
@@ -44,8 +47,9 @@
 // unwritten cache slots (possibly NaN) never meet a zero probability.
 //
 // A one-CTA planning kernel lists the (sequence, 128-row block) work items
-// in decreasing order of key tiles (longest first) in the workspace; the
-// prefill kernel is its programmatic dependent and reads the list after
+// in decreasing order of key tiles (longest first) in the workspace, each as
+// a record of everything a CTA needs to start (offsets, lengths, key tiles);
+// the prefill kernel is its programmatic dependent and reads its record after
 // griddepcontrol.wait, its set-up overlapping the planning.
 #include <math.h>
 

@@ -5,25 +5,36 @@
 // with exact rescaling) and §5.3 (the varlen call, causal=True, and its
 // prefix-cache branch); Lesson 04, §4.
 //
-// Work unit: one CTA per (128 query rows of one sequence, two query heads of
-// one GQA group).  The two heads share every K/V tile the CTA loads, which
-// halves K/V traffic per FLOP compared with one head per CTA.  When the
-// group size is odd a CTA takes one head (the second softmax warpgroup idles).
-// A block of at most 64 rows (a sequence's last block, or a short sequence)
-// carries both heads in one 128-row tile, 64 rows each, so its half-empty
-// rows are not computed twice.
+// Work unit: (128 query rows of one sequence, two query heads of one GQA
+// group).  The two heads share every K/V tile the unit loads, which halves
+// K/V traffic per FLOP compared with one head per unit.  When the group size
+// is odd a unit takes one head (the second softmax warpgroup idles).  A block
+// of at most 64 rows (a sequence's last block, or a short sequence) carries
+// both heads in one 128-row tile, 64 rows each, so its half-empty rows are
+// not computed twice.
 //
-// Roles (320 threads):
+// Persistent CTAs, one per SM, each running units until none is left: a
+// unit's set-up (Q and first K/V loads, first S products) overlaps the
+// previous unit's last tiles and epilogue, and TMEM, barriers and tensor-map
+// prefetches are set up once per SM instead of once per unit.
+//
+// Roles (384 threads; the softmax warpgroups run with 208 registers a thread,
+// the other four warps with 80, by setmaxnreg):
 //   warps 0-3  softmax warpgroup of query head A, thread = query row = TMEM lane
 //   warps 4-7  softmax warpgroup of query head B
-//   warp 8     TMA producer: Q once, then K_0, V_0, K_1, ... (128 keys each)
-//              through a ring of kSlots tiles (packed k/v: one box per 64
-//              columns of head_dim; paged cache: one box per block segment,
-//              addressed via block_tables; blocks shorter than 8 rows are
-//              copied row by row with cp.async into the same layout)
+//   warp 8     producer: per unit K_0, V_0, Q, K_1, V_1, ... (128 keys a
+//              tile) through a ring of kSlots tiles numbered across units
+//              (packed k/v: one TMA box per 64 columns of head_dim; paged
+//              cache: one box per block segment, addressed via block_tables;
+//              blocks shorter than 8 rows are copied row by row with cp.async
+//              into the same layout)
 //   warp 9     MMA issuer (one lane): S_A(0), S_B(0), then per key tile j
 //              P_A(j) V_j, S_A(j+1), P_B(j) V_j, S_B(j+1), so the tensor core
 //              works on one head while the other head's softmax runs
+//   warp 10    idle (completes the third warpgroup for the register split)
+//   warp 11    scheduler (one lane): claims the next unit once the producer
+//              has issued the current one's loads, and publishes units to the
+//              other roles through two shared-memory records
 //
 // Tensor memory (fp32 accumulators, lane = query row), 512 columns: S of
 // head t at 128 t (P, bf16 pairs, written over its upper 64 columns and
@@ -48,9 +59,10 @@
 //
 // A one-CTA planning kernel lists the (sequence, 128-row block) work items
 // in decreasing order of key tiles (longest first) in the workspace, each as
-// a record of everything a CTA needs to start (offsets, lengths, key tiles);
-// the prefill kernel is its programmatic dependent and reads its record after
-// griddepcontrol.wait, its set-up overlapping the planning.
+// a record of everything a unit needs to start (offsets, lengths, key
+// tiles), and zeroes the claim counter; the prefill kernel is its
+// programmatic dependent and reads the list after griddepcontrol.wait, its
+// set-up overlapping the planning.  Units are items x head pairs, item-major.
 #include <math.h>
 
 #include "common.cuh"
@@ -80,9 +92,16 @@ namespace {
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per KV tile
 constexpr int kSlots = 5;         // ring of K / V tiles (K_j, V_j, K_j+1, ...)
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kSchedWarp = 11;   // warp 10 only fills the register-split warpgroup
+constexpr int kUnitSlots = 2;     // published work units (double-buffered)
+constexpr int kUnitUsers = 10;    // roles done with a unit: 8 softmax warps, producer, MMA
+// registers per thread after the split: softmax warpgroups / the other four warps
+// (8*32*208 + 4*32*80 = 63488 <= 384 threads * 168 at launch)
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsOther = 80;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -299,6 +318,7 @@ struct PrefillParams {
     int64_t out_rs;
     float *lse;
     const int32_t *work_count;   // [1]
+    int32_t *claim;              // [1] next unit to claim, less the grid size (zeroed by the plan)
     // [max_items][2]: {sequence, 128-row block, first query row, query rows},
     // {first key row, keys, key tiles, 0} -- everything a CTA needs to start
     const int4 *work;
@@ -363,6 +383,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int
         }
         if (run > p.max_items) atomicOr(&g_prefill_status, PKV_STATUS_BAD_LENGTH);
         *work_count = min(run, p.max_items);
+        *p.claim = 0;
     }
     __syncthreads();
     for (int s = warp; s < p.num_seqs; s += nwarps) {
@@ -390,12 +411,54 @@ struct PLayout {
     static constexpr int kKVTile = H * kBN * 128;           // one K or V tile (a ring slot)
     static constexpr int kOffRing = 2 * kQTile;
     static constexpr int kOffBar = kOffRing + kSlots * kKVTile;
-    static constexpr int kBytes = kOffBar + 256;
+    static constexpr int kOffUnits = kOffBar + 256;         // kUnitSlots work units, 32 bytes each
+    static constexpr int kBytes = kOffBar + 512;
     static constexpr int kTmemCols = 512;
     static constexpr int kColS = 0;                         // S/P of head t at t * kBN
     static constexpr int kColO = 2 * kBN;                   // O of head t at kColO + t * HD
     static_assert(kColO + 2 * HD <= kTmemCols, "tensor memory");
 };
+
+// A work unit as the scheduler warp publishes it: the item's record (see the
+// planning kernel) with the head pair in the last field; a negative head pair
+// ends the CTA's loop.
+struct Unit {
+    int seq, mb, q0, Lq, k0, Lk, n_kv, hp;
+};
+__device__ __forceinline__ Unit read_unit(const int4 *units, int slot) {
+    const int4 a = units[2 * slot], b = units[2 * slot + 1];
+    return Unit{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+}
+
+// Q of a unit: both heads' 128-row tiles, or (packed) both heads' 64 rows in
+// one tile
+template <int HD>
+__device__ __forceinline__ void load_q_tiles(unsigned char *smem, const CUtensorMap *qmap,
+                                             const CUtensorMap *qmap64, uint64_t *q_full, bool packed,
+                                             int pair, int h0, int row0, uint64_t pol) {
+    using L = PLayout<HD>;
+    const int ntile = packed ? 1 : pair;
+    mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * L::kQTile));
+    if (packed) {
+        for (int t = 0; t < 2; ++t)
+            for (int hf = 0; hf < L::H; ++hf)
+                tma_load_3d(smem + hf * kBM * 128 + t * (kBM / 2) * 128, qmap64, q_full, hf * 64, h0 + t,
+                            row0, pol);
+    } else {
+        for (int t = 0; t < ntile; ++t)
+            for (int hf = 0; hf < L::H; ++hf)
+                tma_load_3d(smem + t * L::kQTile + hf * kBM * 128, qmap, q_full, hf * 64, h0 + t, row0, pol);
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void regs_raise() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_lower() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -409,16 +472,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
-    uint64_t *q_full = bars + 0;
-    uint64_t *slot_full = q_full + 1;          // [kSlots] a K or V tile landed
+    uint64_t *q_full = bars + 0;               // Q of the current unit landed
+    uint64_t *q_free = q_full + 1;             // the unit's last S products have read Q
+    uint64_t *slot_full = q_free + 1;          // [kSlots] a K or V tile landed
     uint64_t *slot_free = slot_full + kSlots;  // [kSlots] its MMAs are done with it
     uint64_t *s_full = slot_free + kSlots;     // [2] S of head t in TMEM
     uint64_t *p_full = s_full + 2;             // [2] P of head t in TMEM (4 warp arrivals)
     uint64_t *o_done = p_full + 2;             // [2] P V of head t complete
-    uint64_t *v_fix = o_done + 2;              // last V tile of a paged sequence cleaned
-    uint64_t *drain = v_fix + 1;
+    uint64_t *unit_full = o_done + 2;          // [kUnitSlots] a unit published
+    uint64_t *unit_empty = unit_full + kUnitSlots;   // [kUnitSlots] every role is done with it
+    uint64_t *loads_done = unit_empty + kUnitSlots;  // the producer issued a unit's last load
+    uint64_t *drain = loads_done + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(drain + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int4 *units = reinterpret_cast<int4 *>(smem + L::kOffUnits);
+    static_assert((2 * kSlots + 10 + 2 * kUnitSlots) * 8 + 8 <= L::kOffUnits - L::kOffBar,
+                  "barriers run into the unit records");
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -430,6 +499,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     }
     if (tid == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_free, 1);
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(&slot_full[s], 1);
             mbar_init(&slot_free[s], 1);
@@ -439,7 +509,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(&p_full[t], 4);
             mbar_init(&o_done[t], 1);
         }
-        mbar_init(v_fix, 1);
+        for (int s = 0; s < kUnitSlots; ++s) {
+            mbar_init(&unit_full[s], 1);
+            mbar_init(&unit_empty[s], kUnitUsers);
+        }
+        mbar_init(loads_done, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -454,370 +528,449 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // the work list is written by the planning kernel launched just before
     asm volatile("griddepcontrol.wait;" ::: "memory");
 #endif
-    // the item's record and the item count are read together (one memory
-    // round trip); a record past the count is not used
-    const int item = blockIdx.y;
-    const bool in_range = item < p.max_items;
-    int4 w0 = make_int4(0, 0, 0, 1), w1 = make_int4(0, 1, 1, 0);
-    if (in_range) {
-        w0 = p.work[2 * item];
-        w1 = p.work[2 * item + 1];
-    }
-    const bool idle = !in_range || item >= *p.work_count;              // uniform for the CTA
-    if (idle) {
-        w0 = make_int4(0, 0, 0, 1);
-        w1 = make_int4(0, 1, 1, 0);
-    }
-    const int seq = w0.x, mb = w0.y;
-    const int q0 = w0.z, Lq = w0.w;
-    const int k0 = w1.x, Lk = w1.y;
-    const int off = Lk - Lq;
-    const int r0 = mb * kBM;
-    const int n_kv = w1.z;
-    const int G = p.num_heads / p.num_kv_heads;
-    const int pair = G % 2 == 0 ? 2 : 1;         // two heads of one group, or one head
-    const int h0 = blockIdx.x * pair;
-    const int kvh = h0 / G;
-    // A block with at most 64 query rows (the last block of a sequence, or a
-    // short one) holds both heads in one 128-row tile: head h0 in rows 0..63,
-    // head h0+1 in rows 64..127.  The two heads share every K/V tile, so one
-    // S and one P V stream cover both and the half-empty rows are not computed
-    // twice.
-    const bool packed = PKV_PF_PACK && pair == 2 && Lq - r0 <= kBM / 2;
-    const int ntile = packed ? 1 : pair;
-    auto load_q = [&](uint64_t pol) {
-        mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * L::kQTile));
-        if (packed) {
-            for (int t = 0; t < 2; ++t)
-                for (int hf = 0; hf < H; ++hf)
-                    tma_load_3d(smem + hf * kBM * 128 + t * (kBM / 2) * 128, &qmap64, q_full, hf * 64,
-                                h0 + t, q0 + r0, pol);
-        } else {
-            for (int t = 0; t < ntile; ++t)
-                for (int hf = 0; hf < H; ++hf)
-                    tma_load_3d(smem + t * L::kQTile + hf * kBM * 128, &qmap, q_full, hf * 64, h0 + t,
-                                q0 + r0, pol);
-        }
-    };
-
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    if (idle) {                                  // no work item for this CTA
-        if (warp == kMmaWarp) tmem_dealloc(tmem, L::kTmemCols);
-        return;
-    }
 
-    if (warp == kProducerWarp && p.row_copy) {
-        // ------------------------------------------------------------------
-        // Producer for paged caches whose blocks are shorter than the 8-row
-        // swizzle atom (block_size 1, 2, 4): Q by TMA as usual; each K / V
-        // tile is copied by the whole warp in 16-byte pieces with cp.async,
-        // row by row through block_tables, into the same 128-byte-swizzled
-        // layout a TMA box writes.  Rows past the last key and rows of
-        // missing blocks are zero-filled, so the final tile needs no fix-up.
-        // A tile is published (slot_full) once the next one is in flight:
-        // every lane waits for its own pieces, fences them into the async
-        // proxy that the tensor core reads through, then lane 0 arrives.
-        // ------------------------------------------------------------------
-        if (lane == 0) load_q(policy_evict_first());
-        constexpr int CPR = HD / 8;                  // 16-byte pieces per row
-        const int bs = p.block_size;
-        const int32_t *bt_row = p.bt + (int64_t)seq * p.bt_stride;
-        const int64_t row_elems = (int64_t)p.num_kv_heads * HD;
-        bool live = true;
-        int n = 0;
-        for (; n < 2 * n_kv; ++n) {
-            const int s = n % kSlots;
-            const int j = n >> 1;
-            const uint16_t *cache = (n & 1) ? p.v_cache : p.k_cache;
-            if (n >= kSlots) {
-                int ok = 1;
-                if (lane == 0)
-                    ok = wait_or_abort(&slot_free[s], (uint32_t)((n / kSlots) - 1) & 1u, abort_flag) ? 1 : 0;
-                if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                    live = false;
-                    break;
-                }
-            }
-            const uint32_t dst = smem_u32(smem + L::kOffRing + s * L::kKVTile);
-            bool missing = false;
-            for (int pc = lane; pc < kBN * CPR; pc += 32) {
-                const int r = pc / CPR, cc = pc % CPR;
-                const int pos = j * kBN + r;
-                const uint16_t *src = cache;
-                uint32_t nbytes = 0;
-                if (pos < Lk) {
-                    const int lb = pos / bs;
-                    const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
-                    if (blk >= 0 && blk < p.num_blocks) {
-                        src = cache + ((int64_t)blk * bs + pos % bs) * row_elems + (int64_t)kvh * HD + cc * 8;
-                        nbytes = 16;
-                    } else {
-                        missing = true;
+    const int G = p.num_heads / p.num_kv_heads;
+    const int pair = G % 2 == 0 ? 2 : 1;         // two heads of one group, or one head
+    // A block with at most 64 query rows (the last block of a sequence, or a
+    // short one) holds both heads in one 128-row tile: head h0 in rows 0..63,
+    // head h0+1 in rows 64..127.  The two heads share every K/V tile, so one
+    // S and one P V stream cover both and the half-empty rows are not
+    // computed twice.
+    auto is_packed = [&](const Unit &U) {
+        return PKV_PF_PACK && pair == 2 && U.Lq - U.mb * kBM <= kBM / 2;
+    };
+
+    if (warp >= 8) {
+        // the four single-lane roles give registers to the softmax warpgroups
+        // (one setmaxnreg per warpgroup, executed by all its warps)
+        regs_lower<kRegsOther>();
+        if (warp == kSchedWarp) {
+            // ------------------------------------------------------------------
+            // Scheduler (one lane): the CTA's first unit is its index; each later
+            // one is claimed from a counter once the producer has issued the
+            // current unit's last load (a few tiles before the SM runs out of
+            // work), so units run longest first in about the order the SMs
+            // become free.  A unit is (work item, head pair), items in the
+            // planning kernel's order.
+            // ------------------------------------------------------------------
+            if (lane == 0) {
+                const int npairs = p.num_heads / pair;
+                const int total = *p.work_count * npairs;
+                int unit = blockIdx.x;
+                for (int u = 0;; ++u) {
+                    const int slot = u % kUnitSlots;
+                    if (u > 0) {
+                        if (!wait_or_abort(loads_done, (uint32_t)(u - 1) & 1u, abort_flag)) break;
+                        unit = atomicAdd(p.claim, 1) + (int)gridDim.x;
                     }
+                    int4 a = make_int4(0, 0, 0, 0), b = make_int4(0, 0, 0, -1);
+                    if (unit < total) {
+                        const int item = unit / npairs;
+                        a = p.work[2 * item];
+                        b = p.work[2 * item + 1];
+                        b.w = unit - item * npairs;
+                    }
+                    if (u >= kUnitSlots &&
+                        !wait_or_abort(&unit_empty[slot], (uint32_t)((u / kUnitSlots) - 1) & 1u, abort_flag))
+                        break;
+                    units[2 * slot] = a;
+                    units[2 * slot + 1] = b;
+                    mbar_arrive(&unit_full[slot]);
+                    if (b.w < 0) break;
                 }
-                cp_async16(dst + (uint32_t)((cc / 8) * (kBN * 128) + r * 128 + (((cc % 8) ^ (r & 7)) << 4)),
-                           src, nbytes);
             }
-            cp_async_commit();
-            if (missing && !(n & 1)) atomicOr(&g_prefill_status, PKV_STATUS_BAD_BLOCK);
-            if (n > 0) {
-                cp_async_wait<1>();                  // this lane's pieces of tile n-1 landed
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&slot_full[(n - 1) % kSlots]);
-            }
-        }
-        cp_async_wait<0>();                          // nothing may land after the CTA leaves
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            if (live && n > 0) {
-                mbar_arrive(&slot_full[(n - 1) % kSlots]);
-                if (n_kv * kBN > Lk) mbar_arrive(v_fix);   // the tail rows are zeros already
-            }
-            (void)mbar_wait(q_full, 0);
-        }
-    } else if (warp == kProducerWarp) {
-        // ------------------------------------------------------------------
-        // TMA producer: Q, then the loads K_0, V_0, K_1, V_1, ... into a
-        // ring of kSlots tiles (load n -> slot n % kSlots)
-        // ------------------------------------------------------------------
-        bool issued_all = false;
-        int issued_n = 0;
-        if (lane == 0) {
-            const uint64_t pol_stream = policy_evict_first();
-            load_q(pol_stream);
+        } else if (warp == kProducerWarp && p.row_copy) {
+            // ------------------------------------------------------------------
+            // Producer for paged caches whose blocks are shorter than the 8-row
+            // swizzle atom (block_size 1, 2, 4): Q by TMA as usual; each K / V
+            // tile is copied by the whole warp in 16-byte pieces with cp.async,
+            // row by row through block_tables, into the same 128-byte-swizzled
+            // layout a TMA box writes.  Rows past the last key and rows of
+            // missing blocks are zero-filled, so the final tile needs no fix-up.
+            // A tile is published (slot_full) once the next one is in flight:
+            // every lane waits for its own pieces, fences them into the async
+            // proxy that the tensor core reads through, then lane 0 arrives.
+            // Loads are numbered across the CTA's units (load n -> slot n % kSlots).
+            // ------------------------------------------------------------------
+            constexpr int CPR = HD / 8;                  // 16-byte pieces per row
             const int bs = p.block_size;
-            const int TB = p.paged ? (bs < kBN ? bs : kBN) : kBN;
-            const int32_t *bt_row = p.paged ? p.bt + (int64_t)seq * p.bt_stride : nullptr;
-            int issued = 0;
-            for (int n = 0; n < 2 * n_kv; ++n) {
-                const int s = n % kSlots;
-                const int j = n >> 1;
-                const CUtensorMap *map = (n & 1) ? &vmap : &kmap;
-                if (n >= kSlots &&
-                    !wait_or_abort(&slot_free[s], (uint32_t)((n / kSlots) - 1) & 1u, abort_flag))
-                    break;
-                unsigned char *dst = smem + L::kOffRing + s * L::kKVTile;
-                if (!p.paged) {
-                    mbar_arrive_expect_tx(&slot_full[s], (uint32_t)L::kKVTile);
-                    for (int hf = 0; hf < H; ++hf)
-                        tma_load_3d(dst + hf * kBN * 128, map, &slot_full[s], hf * 64, kvh,
-                                    k0 + j * kBN, pol_stream);
-                } else {
-                    const int nseg = kBN / TB;
-                    int ok = 0;
-                    for (int sg = 0; sg < nseg; ++sg) {
-                        const int pos = j * kBN + sg * TB;
-                        if (pos >= Lk) break;
-                        const int lb = pos / bs;
-                        const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
-                        if (blk >= 0 && blk < p.num_blocks) ++ok;
-                    }
-                    mbar_arrive_expect_tx(&slot_full[s], (uint32_t)(ok * H * TB * 128));
-                    for (int sg = 0; sg < nseg; ++sg) {
-                        const int pos = j * kBN + sg * TB;
-                        if (pos >= Lk) break;
-                        const int lb = pos / bs;
-                        const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
-                        if (blk < 0 || blk >= p.num_blocks) {
-                            if (!(n & 1)) atomicOr(&g_prefill_status, PKV_STATUS_BAD_BLOCK);
-                            continue;
+            const int64_t row_elems = (int64_t)p.num_kv_heads * HD;
+            const uint64_t pol = policy_evict_first();
+            bool live = true;
+            int n = 0, nq = 0;
+            for (int u = 0; live; ++u) {
+                const int slot = u % kUnitSlots;
+                live = wait_or_abort(&unit_full[slot], (uint32_t)(u / kUnitSlots) & 1u, abort_flag);
+                if (!__all_sync(0xffffffffu, live)) { live = false; break; }
+                const Unit U = read_unit(units, slot);
+                if (U.hp < 0) break;
+                const int h0 = U.hp * pair, kvh = h0 / G;
+                const bool packed = is_packed(U);
+                const int32_t *bt_row = p.bt + (int64_t)U.seq * p.bt_stride;
+                // Q after the unit's first K (and V) tile: it waits for the
+                // previous unit's last S products
+                const int q_at = u == 0 ? 0 : min(2, 2 * U.n_kv - 1);
+                for (int i = 0; i < 2 * U.n_kv; ++i, ++n) {
+                    if (i == q_at) {
+                        int ok = 1;
+                        if (lane == 0) {
+                            ok = (u == 0 || wait_or_abort(q_free, (uint32_t)(u - 1) & 1u, abort_flag)) ? 1 : 0;
+                            if (ok) load_q_tiles<HD>(smem, &qmap, &qmap64, q_full, packed, pair, h0, U.q0 + U.mb * kBM, pol);
                         }
-                        const int z = (int)((int64_t)blk * bs + pos % bs);
-                        for (int hf = 0; hf < H; ++hf)
-                            tma_load_3d(dst + hf * kBN * 128 + sg * TB * 128, map, &slot_full[s],
-                                        hf * 64, kvh, z, pol_stream);
+                        if (!__shfl_sync(0xffffffffu, ok, 0)) { live = false; break; }
+                        ++nq;
+                    }
+                    const int s = n % kSlots;
+                    const int j = i >> 1;
+                    const uint16_t *cache = (i & 1) ? p.v_cache : p.k_cache;
+                    if (n >= kSlots) {
+                        int ok = 1;
+                        if (lane == 0)
+                            ok = wait_or_abort(&slot_free[s], (uint32_t)((n / kSlots) - 1) & 1u, abort_flag) ? 1 : 0;
+                        if (!__shfl_sync(0xffffffffu, ok, 0)) { live = false; break; }
+                    }
+                    const uint32_t dst = smem_u32(smem + L::kOffRing + s * L::kKVTile);
+                    bool missing = false;
+                    for (int pc = lane; pc < kBN * CPR; pc += 32) {
+                        const int r = pc / CPR, cc = pc % CPR;
+                        const int pos = j * kBN + r;
+                        const uint16_t *src = cache;
+                        uint32_t nbytes = 0;
+                        if (pos < U.Lk) {
+                            const int lb = pos / bs;
+                            const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
+                            if (blk >= 0 && blk < p.num_blocks) {
+                                src = cache + ((int64_t)blk * bs + pos % bs) * row_elems + (int64_t)kvh * HD + cc * 8;
+                                nbytes = 16;
+                            } else {
+                                missing = true;
+                            }
+                        }
+                        cp_async16(dst + (uint32_t)((cc / 8) * (kBN * 128) + r * 128 + (((cc % 8) ^ (r & 7)) << 4)),
+                                   src, nbytes);
+                    }
+                    cp_async_commit();
+                    if (missing && !(i & 1)) atomicOr(&g_prefill_status, PKV_STATUS_BAD_BLOCK);
+                    if (n > 0) {
+                        cp_async_wait<1>();              // this lane's pieces of load n-1 landed
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&slot_full[(n - 1) % kSlots]);
                     }
                 }
-                ++issued;
-            }
-            issued_n = issued;
-            issued_all = issued == 2 * n_kv;
-        }
-        // paged: zero the value rows past the last key of the final tile once it
-        // has landed, so unwritten cache slots never meet a zero probability
-        const bool fix = __shfl_sync(0xffffffffu, issued_all ? 1 : 0, 0) != 0 && p.paged &&
-                         n_kv * kBN > Lk;
-        if (fix) {
-            const int nv = 2 * n_kv - 1;
-            const int sv = nv % kSlots;
-            const bool ok = wait_or_abort(&slot_full[sv], (uint32_t)(nv / kSlots) & 1u, abort_flag);
-            if (__all_sync(0xffffffffu, ok)) {
-                unsigned char *vt = smem + L::kOffRing + sv * L::kKVTile;
-                const int first = Lk - (n_kv - 1) * kBN;
-                for (int r = first; r < kBN; ++r)
-                    for (int hf = 0; hf < H; ++hf)
-                        *reinterpret_cast<uint32_t *>(vt + hf * kBN * 128 + r * 128 + lane * 4) = 0u;
-                fence_proxy_async_smem();
+                if (!live) break;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(v_fix);
+                if (lane == 0) {
+                    mbar_arrive(loads_done);
+                    mbar_arrive(&unit_empty[slot]);
+                }
             }
-        }
-        if (lane == 0) {
-            // no copy may still be landing when the CTA leaves
-            for (int n = issued_n - kSlots < 0 ? 0 : issued_n - kSlots; n < issued_n; ++n)
-                (void)mbar_wait(&slot_full[n % kSlots], (uint32_t)(n / kSlots) & 1u);
-            (void)mbar_wait(q_full, 0);
-        }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------------
-        // MMA issuer (lane 0).  Order: S_A(0), S_B(0), then per tile j:
-        // P_A(j) V_j, S_A(j+1), P_B(j) V_j, S_B(j+1) -- the tensor core works
-        // on one head while the other head's softmax runs.  P is read from
-        // tensor memory (it overwrites the head's S columns), V and K/Q from
-        // shared memory.
-        // ------------------------------------------------------------------
-        constexpr uint32_t kIdS = idesc_bf16(kBM, kBN, false);
-        constexpr uint32_t kIdO = idesc_bf16(kBM, HD, true);
-        const uint32_t sbase = smem_u32(smem);
-        const uint32_t ring = sbase + L::kOffRing;
-        auto issue_S = [&](int j, int t) {
-            const int s = (2 * j) % kSlots;
-            const uint64_t a0 = sdesc_sw128(sbase + t * L::kQTile, 16, 1024);
-            const uint64_t b0 = sdesc_sw128(ring + s * L::kKVTile, 16, 1024);
+            cp_async_wait<0>();                          // nothing may land after the CTA leaves
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (live && n > 0) mbar_arrive(&slot_full[(n - 1) % kSlots]);
+                if (nq > 0) (void)mbar_wait(q_full, (uint32_t)(nq - 1) & 1u);
+            }
+        } else if (warp == kProducerWarp) {
+            // ------------------------------------------------------------------
+            // TMA producer (one lane): per unit the loads K_0, V_0, K_1, V_1, ...
+            // into a ring of kSlots tiles, numbered across the CTA's units (load
+            // n -> slot n % kSlots); Q of a unit after its first K/V pair, once
+            // the previous unit's last S products have read the Q buffer.
+            // ------------------------------------------------------------------
+            if (lane == 0) {
+                const uint64_t pol = policy_evict_first();
+                const int bs = p.block_size;
+                const int TB = p.paged ? (bs < kBN ? bs : kBN) : kBN;
+                bool live = true;
+                int n = 0, nq = 0;
+                for (int u = 0; live; ++u) {
+                    const int slot = u % kUnitSlots;
+                    if (!wait_or_abort(&unit_full[slot], (uint32_t)(u / kUnitSlots) & 1u, abort_flag)) break;
+                    const Unit U = read_unit(units, slot);
+                    if (U.hp < 0) break;
+                    const int h0 = U.hp * pair, kvh = h0 / G;
+                    const bool packed = is_packed(U);
+                    const int32_t *bt_row = p.paged ? p.bt + (int64_t)U.seq * p.bt_stride : nullptr;
+                    const int q_at = u == 0 ? 0 : min(2, 2 * U.n_kv - 1);
+                    for (int i = 0; i < 2 * U.n_kv; ++i, ++n) {
+                        if (i == q_at) {
+                            if (u > 0 && !wait_or_abort(q_free, (uint32_t)(u - 1) & 1u, abort_flag)) {
+                                live = false;
+                                break;
+                            }
+                            load_q_tiles<HD>(smem, &qmap, &qmap64, q_full, packed, pair, h0, U.q0 + U.mb * kBM, pol);
+                            ++nq;
+                        }
+                        const int s = n % kSlots;
+                        const int j = i >> 1;
+                        const CUtensorMap *map = (i & 1) ? &vmap : &kmap;
+                        if (n >= kSlots &&
+                            !wait_or_abort(&slot_free[s], (uint32_t)((n / kSlots) - 1) & 1u, abort_flag)) {
+                            live = false;
+                            break;
+                        }
+                        unsigned char *dst = smem + L::kOffRing + s * L::kKVTile;
+                        if (!p.paged) {
+                            mbar_arrive_expect_tx(&slot_full[s], (uint32_t)L::kKVTile);
+                            for (int hf = 0; hf < H; ++hf)
+                                tma_load_3d(dst + hf * kBN * 128, map, &slot_full[s], hf * 64, kvh,
+                                            U.k0 + j * kBN, pol);
+                        } else {
+                            const int nseg = kBN / TB;
+                            int ok = 0;
+                            for (int sg = 0; sg < nseg; ++sg) {
+                                const int pos = j * kBN + sg * TB;
+                                if (pos >= U.Lk) break;
+                                const int lb = pos / bs;
+                                const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
+                                if (blk >= 0 && blk < p.num_blocks) ++ok;
+                            }
+                            mbar_arrive_expect_tx(&slot_full[s], (uint32_t)(ok * H * TB * 128));
+                            for (int sg = 0; sg < nseg; ++sg) {
+                                const int pos = j * kBN + sg * TB;
+                                if (pos >= U.Lk) break;
+                                const int lb = pos / bs;
+                                const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
+                                if (blk < 0 || blk >= p.num_blocks) {
+                                    if (!(i & 1)) atomicOr(&g_prefill_status, PKV_STATUS_BAD_BLOCK);
+                                    continue;
+                                }
+                                const int z = (int)((int64_t)blk * bs + pos % bs);
+                                for (int hf = 0; hf < H; ++hf)
+                                    tma_load_3d(dst + hf * kBN * 128 + sg * TB * 128, map, &slot_full[s],
+                                                hf * 64, kvh, z, pol);
+                            }
+                        }
+                    }
+                    if (!live) break;
+                    mbar_arrive(loads_done);
+                    mbar_arrive(&unit_empty[slot]);
+                }
+                // no copy may still be landing when the CTA leaves: every load
+                // before the last kSlots was waited for by the MMA thread before
+                // its slot was released, and every Q before the last one before
+                // q_free
+                for (int m = n - kSlots < 0 ? 0 : n - kSlots; m < n; ++m)
+                    (void)mbar_wait(&slot_full[m % kSlots], (uint32_t)(m / kSlots) & 1u);
+                if (nq > 0) (void)mbar_wait(q_full, (uint32_t)(nq - 1) & 1u);
+            }
+        } else if (warp == kMmaWarp) {
+            // ------------------------------------------------------------------
+            // MMA issuer (lane 0).  Per unit: S_A(0), S_B(0), then per tile j:
+            // P_A(j) V_j, S_A(j+1), P_B(j) V_j, S_B(j+1) -- the tensor core works
+            // on one head while the other head's softmax runs.  P is read from
+            // tensor memory (it overwrites the head's S columns), V and K/Q from
+            // shared memory.  The next unit's first S products follow the last
+            // P V products in the tensor pipe, which has then read every P.
+            // ------------------------------------------------------------------
+            constexpr uint32_t kIdS = idesc_bf16(kBM, kBN, false);
+            constexpr uint32_t kIdO = idesc_bf16(kBM, HD, true);
+            const uint32_t sbase = smem_u32(smem);
+            const uint32_t ring = sbase + L::kOffRing;
+            auto issue_S = [&](int s, int t) {
+                const uint64_t a0 = sdesc_sw128(sbase + t * L::kQTile, 16, 1024);
+                const uint64_t b0 = sdesc_sw128(ring + s * L::kKVTile, 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk) {
-                const uint32_t step = (uint32_t)(((kk / 4) * kBN * 128 + (kk % 4) * 32) >> 4);
-                const uint32_t astep = (uint32_t)(((kk / 4) * kBM * 128 + (kk % 4) * 32) >> 4);
-                umma_bf16(tmem + L::kColS + t * kBN, a0 + astep, b0 + step, kIdS, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&s_full[t]);
-        };
-        auto issue_PV = [&](int j, int t) {
-            const int s = (2 * j + 1) % kSlots;
-            const uint64_t b0 = sdesc_sw128(ring + s * L::kKVTile, kBN * 128, 1024);
-            const uint32_t a_tm = tmem + L::kColS + t * kBN + kColP;   // P: kBN/2 columns
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t step = (uint32_t)(((kk / 4) * kBN * 128 + (kk % 4) * 32) >> 4);
+                    const uint32_t astep = (uint32_t)(((kk / 4) * kBM * 128 + (kk % 4) * 32) >> 4);
+                    umma_bf16(tmem + L::kColS + t * kBN, a0 + astep, b0 + step, kIdS, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&s_full[t]);
+            };
+            auto issue_PV = [&](int s, int t, bool first) {
+                const uint64_t b0 = sdesc_sw128(ring + s * L::kKVTile, kBN * 128, 1024);
+                const uint32_t a_tm = tmem + L::kColS + t * kBN + kColP;   // P: kBN/2 columns
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-                umma_bf16_ts(tmem + L::kColO + t * HD, a_tm + kk * 8, b0 + (uint32_t)((kk * 16 * 128) >> 4),
-                             kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&o_done[t]);
-        };
-        if (lane == 0) {
-            bool live = wait_or_abort(q_full, 0, abort_flag) && wait_or_abort(&slot_full[0], 0, abort_flag);
-            if (live) {
-                tc_fence_after();
-                for (int t = 0; t < ntile; ++t) issue_S(0, t);
-                umma_commit(&slot_free[0]);
-            }
-            for (int j = 0; j < n_kv && live; ++j) {
-                const int nv = 2 * j + 1;                   // load index of V_j
-                const int sv = nv % kSlots;
-                const bool next = j + 1 < n_kv;
-                const int nk = 2 * j + 2;                   // load index of K_{j+1}
-                live = wait_or_abort(&slot_full[sv], (uint32_t)(nv / kSlots) & 1u, abort_flag);
-                if (live && p.paged && !next && (j + 1) * kBN > Lk)
-                    live = wait_or_abort(v_fix, 0, abort_flag);
-                // K_{j+1} too, while the tensor pipe still works through the
-                // previous tile's last S products
-                if (live && next)
-                    live = wait_or_abort(&slot_full[nk % kSlots], (uint32_t)(nk / kSlots) & 1u, abort_flag);
-                for (int t = 0; t < ntile && live; ++t) {
-                    live = wait_or_abort(&p_full[t], (uint32_t)j & 1u, abort_flag);
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    umma_bf16_ts(tmem + L::kColO + t * HD, a_tm + kk * 8, b0 + (uint32_t)((kk * 16 * 128) >> 4),
+                                 kIdO, (!first || kk > 0) ? 1u : 0u);
+                umma_commit(&o_done[t]);
+            };
+            if (lane == 0) {
+                bool live = true;
+                int n0 = 0;                  // load index of the unit's K_0
+                uint32_t ppar = 0;           // bit t: parity of head slot t's tile count
+                for (int u = 0; live; ++u) {
+                    const int slot = u % kUnitSlots;
+                    if (!wait_or_abort(&unit_full[slot], (uint32_t)(u / kUnitSlots) & 1u, abort_flag)) break;
+                    const Unit U = read_unit(units, slot);
+                    if (U.hp < 0) break;
+                    const int ntile = is_packed(U) ? 1 : pair;
+                    live = wait_or_abort(q_full, (uint32_t)u & 1u, abort_flag) &&
+                           wait_or_abort(&slot_full[n0 % kSlots], (uint32_t)(n0 / kSlots) & 1u, abort_flag);
                     if (!live) break;
                     tc_fence_after();
-                    issue_PV(j, t);
-                    if (next) issue_S(j + 1, t);
+                    for (int t = 0; t < ntile; ++t) issue_S(n0 % kSlots, t);
+                    if (U.n_kv == 1) umma_commit(q_free);
+                    umma_commit(&slot_free[n0 % kSlots]);
+                    for (int j = 0; j < U.n_kv && live; ++j) {
+                        const int nv = n0 + 2 * j + 1;              // load index of V_j
+                        const int sv = nv % kSlots;
+                        const bool next = j + 1 < U.n_kv;
+                        const int nk = nv + 1;                      // load index of K_{j+1}
+                        // (a paged unit's last V tile has its rows past the
+                        // last key zeroed by softmax warpgroup 0 before its
+                        // P arrival, which P_A V waits for)
+                        live = wait_or_abort(&slot_full[sv], (uint32_t)(nv / kSlots) & 1u, abort_flag);
+                        // K_{j+1} too, while the tensor pipe still works through
+                        // the previous tile's last S products
+                        if (live && next)
+                            live = wait_or_abort(&slot_full[nk % kSlots], (uint32_t)(nk / kSlots) & 1u, abort_flag);
+                        for (int t = 0; t < ntile && live; ++t) {
+                            live = wait_or_abort(&p_full[t], (ppar >> t) & 1u, abort_flag);
+                            if (!live) break;
+                            ppar ^= 1u << t;
+                            tc_fence_after();
+                            issue_PV(sv, t, j == 0);
+                            if (next) issue_S(nk % kSlots, t);
+                        }
+                        if (live) {
+                            if (j + 2 == U.n_kv) umma_commit(q_free);       // the unit's last S products
+                            umma_commit(&slot_free[sv]);                    // V_j
+                            if (next) umma_commit(&slot_free[nk % kSlots]); // K_{j+1}
+                        }
+                    }
+                    n0 += 2 * U.n_kv;
+                    if (live) mbar_arrive(&unit_empty[slot]);
                 }
-                if (live) {
-                    umma_commit(&slot_free[sv]);                    // V_j
-                    if (next) umma_commit(&slot_free[nk % kSlots]); // K_{j+1}
-                }
+                // every MMA issued by this thread has completed before TMEM is released
+                umma_commit(drain);
+                (void)mbar_wait(drain, 0);
             }
+            __syncwarp();
         }
-        if (lane == 0) {
-            // every MMA issued by this thread has completed before TMEM is released
-            umma_commit(drain);
-            (void)mbar_wait(drain, 0);
-        }
-        __syncwarp();
-    } else if (warp < 8) {
+    } else {
+        regs_raise<kRegsSoftmax>();
         // ------------------------------------------------------------------
-        // softmax warpgroups: thread = query row = TMEM lane
+        // softmax warpgroups: thread = query row = TMEM lane; warpgroup t
+        // takes head h0 + t of each unit (both heads of a packed unit in
+        // warpgroup 0)
         // ------------------------------------------------------------------
         const int t = warp >> 2;
-        if (t < ntile) {
-            const int row = tid & (kBM - 1);
-            // query index within the sequence (packed: rows 64.. are head h0+1)
-            const int qi = r0 + (packed ? (row & (kBM / 2 - 1)) : row);
-            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-            const uint32_t tS = tmem + lane_base + L::kColS + t * kBN;
-            const uint32_t tO = tmem + lane_base + L::kColO + t * HD;
-            const float sc = p.scale_log2;
-            float m = -INFINITY, l = 0.f;
-            bool live = true;
-            for (int j = 0; j < n_kv; ++j) {
-                live = wait_or_abort(&s_full[t], (uint32_t)j & 1u, abort_flag);
-                if (!__all_sync(0xffffffffu, live)) { live = false; break; }
-                tc_fence_after();
-                // scores of the tile, with the causal mask on the tiles that
-                // cross the row's bound
-                const int limit = off + qi - j * kBN;   // columns <= limit are visible
-                uint32_t sr[kBN];
-                tmem_ld128(tS, sr);
-                if (limit < kBN - 1) {
+        const int row = tid & (kBM - 1);
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + L::kColS + t * kBN;
+        const uint32_t tO = tmem + lane_base + L::kColO + t * HD;
+        const float sc = p.scale_log2;
+        uint32_t jpar = 0;              // parity of this head slot's tile count
+        int n0 = 0;                     // load index of the unit's K_0
+        bool live = true;
+        for (int u = 0; live; ++u) {
+            const int slot = u % kUnitSlots;
+            live = wait_or_abort(&unit_full[slot], (uint32_t)(u / kUnitSlots) & 1u, abort_flag);
+            if (!__all_sync(0xffffffffu, live)) { live = false; break; }
+            const Unit U = read_unit(units, slot);
+            if (U.hp < 0) break;
+            const bool packed = is_packed(U);
+            const int ntile = packed ? 1 : pair;
+            const int nv_last = n0 + 2 * U.n_kv - 1;      // load index of the unit's last V tile
+            n0 += 2 * U.n_kv;
+            if (t < ntile) {
+                const int r0 = U.mb * kBM;
+                const int off = U.Lk - U.Lq;
+                // query index within the sequence (packed: rows 64.. are head h0+1)
+                const int qi = r0 + (packed ? (row & (kBM / 2 - 1)) : row);
+                float m = -INFINITY, l = 0.f;
+                for (int j = 0; j < U.n_kv; ++j) {
+                    live = wait_or_abort(&s_full[t], jpar, abort_flag);
+                    if (!__all_sync(0xffffffffu, live)) { live = false; break; }
+                    jpar ^= 1u;
+                    tc_fence_after();
+                    // scores of the tile, with the causal mask on the tiles
+                    // that cross the row's bound
+                    const int limit = off + qi - j * kBN;   // columns <= limit are visible
+                    uint32_t sr[kBN];
+                    tmem_ld128(tS, sr);
+                    if (limit < kBN - 1) {
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c)
-                        if (c > limit) sr[c] = __float_as_uint(-INFINITY);
-                }
-                // row maximum of the raw scores (scale > 0), in four
-                // independent partial maxima; three-input max takes two new
-                // scores per instruction
-                float pm[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    pm[i] = fmaxf(__uint_as_float(sr[i]), __uint_as_float(sr[4 + i]));
-#pragma unroll
-                for (int c = 8; c < kBN; c += 8)
+                        for (int c = 0; c < kBN; ++c)
+                            if (c > limit) sr[c] = __float_as_uint(-INFINITY);
+                    }
+                    // row maximum of the raw scores (scale > 0), in four
+                    // independent partial maxima; three-input max takes two
+                    // new scores per instruction
+                    float pm[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        pm[i] = fmax3(pm[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 4 + i]));
-                const float rmax = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
-                const float m_new = fmaxf(m, rmax * sc);
-                const bool rescale = (m == -INFINITY) ? (m_new != -INFINITY)
-                                                      : (m_new > m + kRescaleThreshold);
-                float alpha = 1.f;
-                if (rescale) {
-                    alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - m_new);
-                    m = m_new;
-                }
-                const float mu = (m == -INFINITY) ? 0.f : m;
-                const bool any_rescale = __any_sync(0xffffffffu, rescale);
-                // p = 2^(s*scale - m), bf16 pairs written over the upper S columns
-                float2 acc[2];
-                exp_pack_store(sr, sc, mu, tS, acc);
-                // S_t(j) follows P_t(j-1) V_{j-1} on the tensor core, so O is
-                // final for the earlier tiles: rescale it in place if needed
-                if (j > 0 && any_rescale) {
-#pragma unroll 1
-                    for (int cc = 0; cc < HD / 32; ++cc) {
-                        float o[32];
-                        tmem_ld32(tO + cc * 32, o);
+                        pm[i] = fmaxf(__uint_as_float(sr[i]), __uint_as_float(sr[4 + i]));
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(tO + cc * 32, o);
+                    for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            pm[i] = fmax3(pm[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 4 + i]));
+                    const float rmax = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+                    const float m_new = fmaxf(m, rmax * sc);
+                    const bool rescale = (m == -INFINITY) ? (m_new != -INFINITY)
+                                                          : (m_new > m + kRescaleThreshold);
+                    float alpha = 1.f;
+                    if (rescale) {
+                        alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - m_new);
+                        m = m_new;
                     }
+                    const float mu = (m == -INFINITY) ? 0.f : m;
+                    const bool any_rescale = __any_sync(0xffffffffu, rescale);
+                    // p = 2^(s*scale - m), bf16 pairs written over the upper S columns
+                    float2 acc[2];
+                    exp_pack_store(sr, sc, mu, tS, acc);
+                    // S_t(j) follows P_t(j-1) V_{j-1} on the tensor core, so O
+                    // is final for the earlier tiles: rescale it in place if needed
+                    if (j > 0 && any_rescale) {
+#pragma unroll 1
+                        for (int cc = 0; cc < HD / 32; ++cc) {
+                            float o[32];
+                            tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                            tmem_st32(tO + cc * 32, o);
+                        }
+                    }
+                    l *= alpha;
+                    tmem_wait_st();
+                    l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+                    if (t == 0 && j + 1 == U.n_kv && p.paged && !p.row_copy && U.n_kv * kBN > U.Lk) {
+                        // paged cache by TMA boxes: zero the value rows past the
+                        // last key of the final V tile once it has landed, so
+                        // unwritten cache slots (possibly NaN) never meet a zero
+                        // probability.  S of this tile has landed, so every
+                        // earlier load of the slot was waited for by the MMA
+                        // thread, and the slot is not refilled before the P V
+                        // products that follow this arrival: the parity below
+                        // names this load's phase.
+                        const int sv = nv_last % kSlots;
+                        live = wait_or_abort(&slot_full[sv], (uint32_t)(nv_last / kSlots) & 1u, abort_flag);
+                        if (!__all_sync(0xffffffffu, live)) { live = false; break; }
+                        unsigned char *vt = smem + L::kOffRing + sv * L::kKVTile;
+                        const int first = U.Lk - (U.n_kv - 1) * kBN;
+                        const int pieces = (kBN - first) * 8;      // 16-byte pieces per 128-byte half
+                        for (int c = row; c < H * pieces; c += kBM) {
+                            const int hf = c / pieces, rc = c % pieces;
+                            *reinterpret_cast<uint4 *>(vt + hf * kBN * 128 + (first + rc / 8) * 128 + (rc % 8) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[t]);
                 }
-                l *= alpha;
-                tmem_wait_st();
-                l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[t]);
-            }
-            // epilogue: O / l -> bf16 rows, lse
-            if (live)
-                live = wait_or_abort(&o_done[t], (uint32_t)(n_kv - 1) & 1u, abort_flag);
-            if (__all_sync(0xffffffffu, live)) {
+                if (!live) break;
+                // epilogue: O / l -> bf16 rows, lse.  The tensor memory read
+                // here is complete before this warp's next P arrival, which
+                // the next unit's first P V product (overwriting O) waits for.
+                live = wait_or_abort(&o_done[t], jpar ^ 1u, abort_flag);
+                if (!__all_sync(0xffffffffu, live)) { live = false; break; }
                 tc_fence_after();
-                const bool row_ok = qi < Lq;
+                const bool row_ok = qi < U.Lq;
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                const int hq = packed ? h0 + (row >> 6) : h0 + t;
-                uint16_t *orow = p.out + (int64_t)(q0 + (row_ok ? qi : 0)) * p.out_rs + (int64_t)hq * HD;
+                const int hq = U.hp * pair + (packed ? (row >> 6) : t);
+                uint16_t *orow = p.out + (int64_t)(U.q0 + (row_ok ? qi : 0)) * p.out_rs + (int64_t)hq * HD;
                 uint32_t ov[HD];
                 tmem_ld_row<HD>(tO, ov);
                 if (row_ok) {
@@ -832,9 +985,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     }
                 }
                 if (row_ok && p.lse)
-                    p.lse[(int64_t)(q0 + qi) * p.num_heads + hq] =
+                    p.lse[(int64_t)(U.q0 + qi) * p.num_heads + hq] =
                         l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&unit_empty[slot]);
         }
     }
 
@@ -865,23 +1020,37 @@ int launch_hd(const PrefillArgs &a, const PrefillParams &pp, int4 *work, int32_t
         if (!rc) rc = encode_rows_heads_map(&vm, a.v, a.total_k, a.num_kv_heads, HD, a.v_rs, HD, 64, kBN, true, err);
     }
     if (rc) return rc;
-    prefill_plan_kernel<<<1, 1024, 0, stream>>>(pp, count, work);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
     const int smem = L::kBytes + 1024;
     auto kern = prefill_kernel<HD>;
     static PerDeviceOnce once;
     int dev = 0;
-    e = cudaGetDevice(&dev);
+    cudaError_t e = cudaGetDevice(&dev);
+    bool regs_ok = true;
     if (e == cudaSuccess)
         e = once.run(dev, [&]() {
-            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            // the register split (setmaxnreg) redistributes the registers the
+            // CTA is launched with; it must not ask for more than that
+            cudaFuncAttributes fa;
+            cudaError_t r = cudaFuncGetAttributes(&fa, kern);
+            if (r == cudaSuccess &&
+                fa.numRegs * kThreads < 8 * 32 * kRegsSoftmax + 4 * 32 * kRegsOther)
+                return cudaErrorInvalidConfiguration;
+            if (r == cudaSuccess)
+                r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            return r;
         });
+    if (e == cudaErrorInvalidConfiguration) regs_ok = false;
+    if (!regs_ok) { *err = "prefill kernel compiled with fewer registers than its register split needs"; return PKV_ERR_CUDA; }
+    if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
+    prefill_plan_kernel<<<1, 1024, 0, stream>>>(pp, count, work);
+    e = cudaGetLastError();
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
     const int G = a.num_heads / a.num_kv_heads;
     const int pair = G % 2 == 0 ? 2 : 1;
+    const int64_t max_units = (int64_t)max_items * (a.num_heads / pair);
+    const int grid = (int)(max_units < num_sms() ? max_units : num_sms());
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.num_heads / pair, max_items);
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -925,7 +1094,7 @@ int launch_prefill(const PrefillArgs &a, cudaStream_t stream, const char **err) 
         return PKV_ERR_WORKSPACE;
     }
     const int max_items = max_work_items(a.num_seqs, a.total_q);
-    if (max_items > 65535) {
+    if ((int64_t)max_items * a.num_heads > (int64_t)1 << 30) {
         *err = "too many 128-row query blocks for one launch";
         return PKV_ERR_UNSUPPORTED;
     }
@@ -948,6 +1117,7 @@ int launch_prefill(const PrefillArgs &a, cudaStream_t stream, const char **err) 
     pp.out_rs = a.out_rs;
     pp.lse = a.lse;
     pp.work_count = count;
+    pp.claim = count + 1;
     pp.work = work;
     pp.max_items = max_items;
     pp.row_copy = paged && a.block_size < 8 ? 1 : 0;

@@ -110,6 +110,9 @@ constexpr int kColP = kBN / 2;
 #ifndef PKV_PF_PDL
 #define PKV_PF_PDL 1   // prefill kernel launched as a programmatic dependent of the planning kernel
 #endif
+#ifndef PKV_PF_OUT_V8
+#define PKV_PF_OUT_V8 1   // 32-byte output stores when the output rows are 32-byte aligned
+#endif
 #ifndef PKV_PF_PACK
 #define PKV_PF_PACK 1   // blocks of at most 64 rows carry both heads of a pair in one tile
 #endif    // P (bf16 pairs) over the upper half of a head's S columns
@@ -327,6 +330,7 @@ struct PrefillParams {
     // are copied row by row from the caches instead of by TMA boxes
     int32_t row_copy;
     const uint16_t *k_cache, *v_cache;
+    int32_t out_v8;              // out and its row stride allow 32-byte stores
 };
 
 __device__ __forceinline__ int kv_tiles_for(int Lq, int Lk, int mb) {
@@ -449,6 +453,21 @@ __device__ __forceinline__ void load_q_tiles(unsigned char *smem, const CUtensor
             for (int hf = 0; hf < L::H; ++hf)
                 tma_load_3d(smem + t * L::kQTile + hf * kBM * 128, qmap, q_full, hf * 64, h0 + t, row0, pol);
     }
+}
+
+// L2 policy of the K/V tile loads: every later block of the sequence reads
+// the same tiles (Q, read once, keeps evict_first)
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 32 bytes to global memory, streaming (written once)
+__device__ __forceinline__ void st_cs_v8(void *p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
 }
 
 template <int N>
@@ -685,6 +704,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             // ------------------------------------------------------------------
             if (lane == 0) {
                 const uint64_t pol = policy_evict_first();
+                const uint64_t kvpol = policy_evict_normal();
                 const int bs = p.block_size;
                 const int TB = p.paged ? (bs < kBN ? bs : kBN) : kBN;
                 bool live = true;
@@ -720,7 +740,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                             mbar_arrive_expect_tx(&slot_full[s], (uint32_t)L::kKVTile);
                             for (int hf = 0; hf < H; ++hf)
                                 tma_load_3d(dst + hf * kBN * 128, map, &slot_full[s], hf * 64, kvh,
-                                            U.k0 + j * kBN, pol);
+                                            U.k0 + j * kBN, kvpol);
                         } else {
                             const int nseg = kBN / TB;
                             int ok = 0;
@@ -744,7 +764,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                 const int z = (int)((int64_t)blk * bs + pos % bs);
                                 for (int hf = 0; hf < H; ++hf)
                                     tma_load_3d(dst + hf * kBN * 128 + sg * TB * 128, map, &slot_full[s],
-                                                hf * 64, kvh, z, pol);
+                                                hf * 64, kvh, z, kvpol);
                             }
                         }
                     }
@@ -973,7 +993,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 uint16_t *orow = p.out + (int64_t)(U.q0 + (row_ok ? qi : 0)) * p.out_rs + (int64_t)hq * HD;
                 uint32_t ov[HD];
                 tmem_ld_row<HD>(tO, ov);
-                if (row_ok) {
+                if (row_ok && PKV_PF_OUT_V8 && p.out_v8) {
+#pragma unroll
+                    for (int v = 0; v < HD / 16; ++v) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            w[e] = pack_bf16x2(__uint_as_float(ov[v * 16 + 2 * e]) * inv,
+                                               __uint_as_float(ov[v * 16 + 2 * e + 1]) * inv);
+                        st_cs_v8(orow + v * 16, w);   // written once
+                    }
+                } else if (row_ok) {
 #pragma unroll
                     for (int v = 0; v < HD / 8; ++v) {
                         uint4 pkt;
@@ -1121,6 +1151,7 @@ int launch_prefill(const PrefillArgs &a, cudaStream_t stream, const char **err) 
     pp.work = work;
     pp.max_items = max_items;
     pp.row_copy = paged && a.block_size < 8 ? 1 : 0;
+    pp.out_v8 = (reinterpret_cast<uintptr_t>(a.out) % 32 == 0 && a.out_rs % 16 == 0) ? 1 : 0;
     pp.k_cache = a.k_cache;
     pp.v_cache = a.v_cache;
     if (a.head_dim == 128) return launch_hd<128>(a, pp, work, count, max_items, stream, err);

@@ -36,12 +36,13 @@ def _built():
     ops.device_status(clear=True)
 
 
-def _guarded_out(rows, heads, d):
+def _guarded_out(rows, heads, d, shift=0):
     """(buffer, view): the view is [rows, heads, d] at row 1 of a canary-filled
-    buffer whose rows are heads*d + PAD elements long."""
+    buffer whose rows are heads*d + PAD elements long, starting `shift`
+    elements into the row (8: rows 16-byte but not 32-byte aligned)."""
     width = heads * d + PAD
     buf = torch.full((rows + 2, width), NAN_BITS, dtype=torch.int16, device="cuda").view(torch.bfloat16)
-    view = buf[1:rows + 1, :heads * d].view(rows, heads, d)
+    view = buf[1:rows + 1, shift:shift + heads * d].view(rows, heads, d)
     assert view.stride(0) == width
     return buf, view
 
@@ -51,10 +52,11 @@ def _guarded_lse(rows, heads):
     return buf, buf[:rows * heads].view(rows, heads)
 
 
-def _canary_intact(buf, rows, heads, d):
+def _canary_intact(buf, rows, heads, d, shift=0):
     b = buf.view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.all(b[0] == NAN_BITS) and np.all(b[rows + 1] == NAN_BITS), "pad rows written"
-    assert np.all(b[1:rows + 1, heads * d:] == NAN_BITS), "row gaps written"
+    assert np.all(b[1:rows + 1, :shift] == NAN_BITS), "row gaps written"
+    assert np.all(b[1:rows + 1, shift + heads * d:] == NAN_BITS), "row gaps written"
 
 
 def _status_of(err) -> int:
@@ -67,13 +69,16 @@ def _lse_canary_intact(buf, rows, heads):
     assert torch.isnan(buf[rows * heads:]).all(), "elements past the lse written"
 
 
+@pytest.mark.parametrize("shift", [0, 8], ids=["aligned32", "aligned16"])
 @pytest.mark.parametrize("paged", [False, True])
-def test_prefill_writes_only_its_rows(paged):
+def test_prefill_writes_only_its_rows(paged, shift):
+    """Output rows 32-byte aligned (32-byte stores) and only 16-byte aligned
+    (16-byte stores)."""
     heads = W.Heads(16, 8, 128, 64, 96)
     lens, prefix = [1, 129, 300, 64], ([0, 70, 128, 5] if paged else None)
     work = W.prefill_work(heads, lens, prefix, seed=910 + paged)
     n = work.total_q
-    obuf, out = _guarded_out(n, heads.num_heads, heads.head_dim)
+    obuf, out = _guarded_out(n, heads.num_heads, heads.head_dim, shift)
     lbuf, lse = _guarded_lse(n, heads.num_heads)
     if paged:
         kc, vc = W.history_cache(heads, 911)
@@ -101,7 +106,7 @@ def test_prefill_writes_only_its_rows(paged):
                                dev(work.cu_seqlens_k), work.max_seqlen_q, work.max_seqlen_k,
                                heads.scale, out=out, lse=lse)
     torch.cuda.synchronize()
-    _canary_intact(obuf, n, heads.num_heads, heads.head_dim)
+    _canary_intact(obuf, n, heads.num_heads, heads.head_dim, shift)
     _lse_canary_intact(lbuf, n, heads.num_heads)
     assert_close(out, ref, "prefill rows inside the guard bands")
     assert np.allclose(lse.cpu().double().numpy(), ref_lse, atol=2e-3, rtol=1e-4)

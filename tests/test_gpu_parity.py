@@ -476,6 +476,24 @@ def test_prefill_odd_groups(hq, hkv, d):
     _prefill_paged(heads, [150, 40], [64 + 3, 0], seed=650 + hq)
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (6, 2, 64)])
+def test_prefill_one_head_units_long(hq, hkv, d):
+    """Groups 1 and 3 (one head per work unit) on long sequences with odd and
+    even key-tile counts, packed and prefix-cache, and scores that grow
+    along the keys (the running maximum moves late)."""
+    _prefill_packed(W.Heads(hq, hkv, d, 16, 256), [1000, 513, 64, 1], seed=680 + hq)
+    heads = W.Heads(hq, hkv, d, 64, 96)
+    _prefill_paged(heads, [300, 65, 640], [1000, 7, 129], seed=690 + hq)
+    _prefill_paged(heads, [200, 640], [900, 0], seed=695 + hq, growing=True)
+
+
+def test_prefill_packed_blocks_long_prefix():
+    """Blocks of at most 64 rows (both heads of a pair in one tile) behind a
+    long cached prefix: many key tiles for one packed tile stream."""
+    heads = W.Heads(16, 8, 128, 256, 48)
+    _prefill_paged(heads, [60, 7, 192 + 33], [2048 + 100, 777, 1500], seed=710)
+
+
 def test_prefill_paged_group4_d64():
     heads = W.Heads(16, 4, 64, 32, 64)
     _prefill_paged(heads, [90, 200], [40, 0], seed=780)

@@ -106,6 +106,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr int kCostBins = 2048;
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanSeqs = 1024;   // sequences whose lengths the planning kernel keeps on chip
 constexpr int kColP = kBN / 2;
 #ifndef PKV_PF_PDL
 #define PKV_PF_PDL 1   // prefill kernel launched as a programmatic dependent of the planning kernel
@@ -341,32 +343,27 @@ __device__ __forceinline__ int kv_tiles_for(int Lq, int Lk, int mb) {
 
 // Work list: every (sequence, 128-row block), ordered by decreasing number
 // of key tiles (a counting sort on the cost).  One CTA: a warp per sequence,
-// lanes over its row blocks; the scan runs over the bins in use only.
-__global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int32_t *work_count,
+// lanes over its row blocks; one warp scans the bins in use, 32 at a time.
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PrefillParams p, int32_t *work_count,
                                                             int4 *work) {
     __shared__ int hist[kCostBins];
     __shared__ int top;                         // highest cost bin in use
+    __shared__ int4 seqs[kPlanSeqs];            // {first query row, query rows, first key row, keys}
 #if PKV_PF_PDL
     // the prefill kernel may start its set-up now; it waits for this grid
     // (and its writes) before reading the work list
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    // the lengths of this warp's first sequence, kept for the second pass
-    const int s_first = warp < p.num_seqs ? warp : -1;
-    int f_q0 = 0, f_q1 = 0, f_k0 = 0, f_k1 = 0;
-    if (s_first >= 0) {
-        f_q0 = p.cu_q[s_first];
-        f_q1 = p.cu_q[s_first + 1];
-        f_k0 = p.cu_k[s_first];
-        f_k1 = p.cu_k[s_first + 1];
-    }
     for (int i = threadIdx.x; i < kCostBins; i += blockDim.x) hist[i] = 0;
     if (threadIdx.x == 0) top = 0;
     __syncthreads();
+    // pass 1: cost histogram; each sequence's offsets and lengths are kept
+    // for pass 2 (in shared memory for the first kPlanSeqs sequences)
     for (int s = warp; s < p.num_seqs; s += nwarps) {
-        const int Lq = s == s_first ? f_q1 - f_q0 : p.cu_q[s + 1] - p.cu_q[s];
-        const int Lk = s == s_first ? f_k1 - f_k0 : p.cu_k[s + 1] - p.cu_k[s];
+        const int q0 = p.cu_q[s], k0 = p.cu_k[s];
+        const int Lq = p.cu_q[s + 1] - q0, Lk = p.cu_k[s + 1] - k0;
+        if (s < kPlanSeqs && lane == 0) seqs[s] = make_int4(q0, Lq, k0, Lk);
         if (Lq <= 0) continue;
         if (Lk < Lq) {
             if (lane == 0) atomicOr(&g_prefill_status, PKV_STATUS_BAD_LENGTH);
@@ -378,23 +375,38 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int
         if (lane == 0) atomicMax(&top, min(kv_tiles_for(Lq, Lk, nmb - 1), kCostBins - 1));
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;   // descending cost: bins from high to low
-        for (int c = top; c >= 0; --c) {
-            const int h = hist[c];
-            hist[c] = run;
-            run += h;
+    if (warp == 0) {
+        // exclusive prefix sums in descending cost: each bin's first position
+        int run = 0;
+        for (int hi = top; hi >= 0; hi -= 32) {
+            const int c = hi - lane;                    // lane 0: the chunk's highest bin
+            const int h = c >= 0 ? hist[c] : 0;
+            int x = h;                                  // inclusive scan over the lanes
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (c >= 0) hist[c] = run + x - h;
+            run += __shfl_sync(0xffffffffu, x, 31);
         }
-        if (run > p.max_items) atomicOr(&g_prefill_status, PKV_STATUS_BAD_LENGTH);
-        *work_count = min(run, p.max_items);
-        *p.claim = 0;
+        if (lane == 0) {
+            if (run > p.max_items) atomicOr(&g_prefill_status, PKV_STATUS_BAD_LENGTH);
+            *work_count = min(run, p.max_items);
+            *p.claim = 0;
+        }
     }
     __syncthreads();
+    // pass 2: each item's record at the next position of its cost bin
     for (int s = warp; s < p.num_seqs; s += nwarps) {
-        const int q0 = s == s_first ? f_q0 : p.cu_q[s];
-        const int k0 = s == s_first ? f_k0 : p.cu_k[s];
-        const int Lq = (s == s_first ? f_q1 : p.cu_q[s + 1]) - q0;
-        const int Lk = (s == s_first ? f_k1 : p.cu_k[s + 1]) - k0;
+        int4 sq;
+        if (s < kPlanSeqs) {
+            sq = seqs[s];
+        } else {
+            const int q0 = p.cu_q[s], k0 = p.cu_k[s];
+            sq = make_int4(q0, p.cu_q[s + 1] - q0, k0, p.cu_k[s + 1] - k0);
+        }
+        const int q0 = sq.x, Lq = sq.y, k0 = sq.z, Lk = sq.w;
         if (Lq <= 0 || Lk < Lq) continue;
         const int nmb = (Lq + kBM - 1) / kBM;
         for (int mb = lane; mb < nmb; mb += 32) {
@@ -1072,7 +1084,7 @@ int launch_hd(const PrefillArgs &a, const PrefillParams &pp, int4 *work, int32_t
     if (e == cudaErrorInvalidConfiguration) regs_ok = false;
     if (!regs_ok) { *err = "prefill kernel compiled with fewer registers than its register split needs"; return PKV_ERR_CUDA; }
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
-    prefill_plan_kernel<<<1, 1024, 0, stream>>>(pp, count, work);
+    prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pp, count, work);
     e = cudaGetLastError();
     if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
     const int G = a.num_heads / a.num_kv_heads;

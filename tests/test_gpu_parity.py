@@ -413,6 +413,16 @@ def test_prefill_packed_vs_oracle(shape):
     _prefill_packed(W.Heads(hq, hkv, d, 16, 256), lens, seed=600 + hq + d + len(lens))
 
 
+def test_prefill_many_sequences():
+    """More sequences than the planning kernel keeps on chip (1024): the
+    lengths of the rest are read again from cu_seqlens in its second pass;
+    short sequences, empty ones among them."""
+    g = W.generator(9100)
+    lens = torch.randint(0, 6, (1300,), generator=g).tolist()
+    lens[1100] = 300
+    _prefill_packed(W.Heads(4, 2, 64, 16, 4096), lens, seed=9101)
+
+
 def test_prefill_fused_qkv_views():
     _prefill_packed(W.Heads(16, 8, 128, 16, 256), [300, 77], seed=650, fused=True)
 

@@ -743,11 +743,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         if (aborted) break;                         // uniform, after the last barrier
         g0 += it.ntiles;
     }
+    // the merge kernel (a programmatic dependent) may be scheduled once every
+    // CTA of this one resident wave has got here; it waits for this grid's
+    // completion before it reads the partials
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Merge the chunks of each (sequence, head): one warp per pair.
 template <int HD>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
+    // launched as the split kernel's programmatic dependent: its partials
+    // are complete and visible after this wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hq = blockIdx.x * 4 + warp;
     const int b = blockIdx.y;
@@ -913,12 +920,18 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream, const char **err) {
                 : dispatch_group<64, false>(G, km, vm, p, a.batch, a.num_kv_heads, stream, err);
     if (rc) return rc;
     if (splits > 1) {
-        dim3 grid((a.num_heads + 3) / 4, a.batch);
-        if (a.head_dim == 128)
-            decode_combine_kernel<128><<<grid, 128, 0, stream>>>(p);
-        else
-            decode_combine_kernel<64><<<grid, 128, 0, stream>>>(p);
-        cudaError_t e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((a.num_heads + 3) / 4, a.batch);
+        cfg.blockDim = dim3(128);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = a.head_dim == 128 ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, p)
+                                          : cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, p);
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) { *err = cudaGetErrorString(e); return PKV_ERR_CUDA; }
     }
     return PKV_OK;

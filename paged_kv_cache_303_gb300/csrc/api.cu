@@ -519,9 +519,12 @@ int paged_attn_prefill(const pkv_bf16 *q, int64_t q_row_stride, const pkv_bf16 *
 }  // extern "C"
 
 #if PKV_TEST_HOOKS
-// Only in the test-only build (never in libpagedkv.so): see decode.cu.
+// Only in the test-only build (never in libpagedkv.so): see decode.cu and
+// prefill.cu.
 namespace pkv {
 int test_withhold_decode_ready(int on);
+int test_withhold_prefill_unit(int on);
 }
 extern "C" int pkv_test_withhold_decode_ready(int on) { return pkv::test_withhold_decode_ready(on); }
+extern "C" int pkv_test_withhold_prefill_unit(int on) { return pkv::test_withhold_prefill_unit(on); }
 #endif

@@ -72,6 +72,18 @@ namespace pkv {
 
 static __device__ unsigned int g_prefill_status;
 
+#if PKV_TEST_HOOKS
+// Test-only build: while set, the scheduler of CTA 0 publishes no unit at
+// all, so that CTA's other roles wait on the first unit record until the
+// bound runs out.  Nothing has been issued by then (no copy, no tensor-core
+// product), so every role leaves with nothing in flight.
+static __device__ int g_test_withhold_prefill_unit;
+
+int test_withhold_prefill_unit(int on) {
+    return cudaMemcpyToSymbol(g_test_withhold_prefill_unit, &on, sizeof on) == cudaSuccess ? 0 : -1;
+}
+#endif
+
 cudaError_t prefill_status(cudaStream_t stream, uint32_t *host, bool clear) {
     unsigned int v = 0;
     cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_prefill_status, sizeof v, 0,
@@ -608,6 +620,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     if (u >= kUnitSlots &&
                         !wait_or_abort(&unit_empty[slot], (uint32_t)((u / kUnitSlots) - 1) & 1u, abort_flag))
                         break;
+#if PKV_TEST_HOOKS
+                    if (u == 0 && blockIdx.x == 0 && g_test_withhold_prefill_unit) break;
+#endif
                     units[2 * slot] = a;
                     units[2 * slot + 1] = b;
                     mbar_arrive(&unit_full[slot]);

@@ -28,13 +28,22 @@ when the open phase's parity is not P. It checks that:
   * the epilogue reads O after all of the unit's P V products;
   * the zeroing of a paged unit's last V tile hits that tile after it has
     landed and before its P V;
-  * nothing deadlocks, and no copy is landing when the CTA ends.
+  * nothing deadlocks;
+  * when the CTA ends, no copy is landing and no product or commit is
+    pending.
 
-Three planted mistakes are caught. The first is a separate warp that zeroes
+Every wait of a role but the teardown's gives up once the CTA's abort flag
+is raised (the kernel raises it when a bounded wait runs out).  Runs that
+raise it at a random step check that each role leaves by its own exit path
+and that the teardown still waits for every copy and product it issued.
+
+Five planted mistakes are caught. The first is a separate warp that zeroes
 the V tail without the softmax's ordering. The second is a softmax whose S
 parity restarts with every unit instead of running on across units. The
 third has the producer skip the wait for the previous unit's last S
-products before reloading Q.
+products before reloading Q. The fourth and fifth leave after an abort
+without the teardown: a producer that does not wait for its copies and an
+MMA thread that does not wait for its products.
 """
 import random
 
@@ -72,12 +81,32 @@ class Bar:
         return (self.phase & 1) != parity
 
 
-def simulate(units, rng, plant=None, units_per_tile=2):
+class W:
+    """A wait that gives up when the CTA's abort flag is raised (the kernel's
+    wait_or_abort): the role receives True if the phase completed, False if
+    it gave up."""
+
+    def __init__(self, pred):
+        self.pred = pred
+
+
+class P:
+    """A plain wait (bounded only by time): the teardown waits for copies and
+    products that are already issued."""
+
+    def __init__(self, pred):
+        self.pred = pred
+
+
+def simulate(units, rng, plant=None, units_per_tile=2, abort_at=None):
     """units: list of (n_kv, ntile, tail); tail: paged unit whose last V tile
-    has rows past the last key.  Returns the list of violations."""
+    has rows past the last key.  abort_at: scheduling step at which the CTA's
+    abort flag is raised (as when some wait of the CTA ran out of time).
+    Returns the list of violations."""
     log = []
     B = lambda n, c=1: Bar(c, log, n)
     q_full, q_free, loads_done = B("q_full"), B("q_free"), B("loads_done")
+    drain = B("drain")
     slot_full = [B(f"slot_full{s}") for s in range(K_SLOTS)]
     slot_free = [B(f"slot_free{s}") for s in range(K_SLOTS)]
     s_full = [B(f"s_full{t}") for t in range(2)]
@@ -87,6 +116,7 @@ def simulate(units, rng, plant=None, units_per_tile=2):
     unit_empty = [B(f"unit_empty{i}", 4) for i in range(2)]   # producer, MMA, two softmax groups
     records = [None, None]
     total_units = len(units)
+    abort = [False]
 
     slot = [None] * K_SLOTS            # [load index, landed units, zeroed] in the stage
     q_buf = [None]                     # [unit, landed units]
@@ -100,17 +130,21 @@ def simulate(units, rng, plant=None, units_per_tile=2):
     def scheduler():
         for u in range(total_units + 1):
             if u >= 1:
-                yield lambda u=u: loads_done.try_wait_parity((u - 1) & 1)
+                if not (yield W(lambda u=u: loads_done.try_wait_parity((u - 1) & 1))):
+                    return
             if u >= 2:
-                yield lambda u=u: unit_empty[u % 2].try_wait_parity(((u // 2) - 1) & 1)
+                if not (yield W(lambda u=u: unit_empty[u % 2].try_wait_parity(((u // 2) - 1) & 1))):
+                    return
             records[u % 2] = units[u] if u < total_units else None
             unit_full[u % 2].arrive()
             yield None
 
     def producer():
         n, nq = 0, 0
+        live = True
         for u in range(total_units + 1):
-            yield lambda u=u: unit_full[u % 2].try_wait_parity((u // 2) & 1)
+            if not (yield W(lambda u=u: unit_full[u % 2].try_wait_parity((u // 2) & 1))):
+                break
             rec = records[u % 2]
             if rec is None:
                 break
@@ -119,7 +153,9 @@ def simulate(units, rng, plant=None, units_per_tile=2):
             for i in range(2 * n_kv):
                 if i == q_at:
                     if u > 0 and plant != "no_q_free_wait":
-                        yield lambda u=u: q_free.try_wait_parity((u - 1) & 1)
+                        if not (yield W(lambda u=u: q_free.try_wait_parity((u - 1) & 1))):
+                            live = False
+                            break
                     if q_readers[0]:
                         log.append(f"Q of unit {u} loaded while a product still reads unit {q_buf[0][0]}'s")
                     q_full.arrive_expect_tx(units_per_tile)
@@ -129,7 +165,9 @@ def simulate(units, rng, plant=None, units_per_tile=2):
                     yield None
                 s = n % K_SLOTS
                 if n >= K_SLOTS:
-                    yield lambda s=s, n=n: slot_free[s].try_wait_parity(((n // K_SLOTS) - 1) & 1)
+                    if not (yield W(lambda s=s, n=n: slot_free[s].try_wait_parity(((n // K_SLOTS) - 1) & 1))):
+                        live = False
+                        break
                 if readers[s]:
                     log.append(f"stage {s} refilled with load {n} while a product reads it")
                 if any(c[0] == "kv" and c[1] == s for c in inflight):
@@ -139,12 +177,17 @@ def simulate(units, rng, plant=None, units_per_tile=2):
                 inflight.extend([("kv", s, n)] * units_per_tile)
                 n += 1
                 yield None
+            if not live:
+                break
             loads_done.arrive()
             unit_empty[u % 2].arrive()
+        if plant == "no_copy_drain":
+            return
+        # no copy may still be landing when the CTA leaves
         for m in range(max(0, n - K_SLOTS), n):
-            yield lambda m=m: slot_full[m % K_SLOTS].try_wait_parity((m // K_SLOTS) & 1)
+            yield P(lambda m=m: slot_full[m % K_SLOTS].try_wait_parity((m // K_SLOTS) & 1))
         if nq:
-            yield lambda: q_full.try_wait_parity((nq - 1) & 1)
+            yield P(lambda: q_full.try_wait_parity((nq - 1) & 1))
 
     def use_slot(n, what):
         s = n % K_SLOTS
@@ -157,13 +200,16 @@ def simulate(units, rng, plant=None, units_per_tile=2):
         n0 = 0
         ppar = [0, 0]
         for u in range(total_units + 1):
-            yield lambda u=u: unit_full[u % 2].try_wait_parity((u // 2) & 1)
+            if not (yield W(lambda u=u: unit_full[u % 2].try_wait_parity((u // 2) & 1))):
+                break
             rec = records[u % 2]
             if rec is None:
                 break
             n_kv, ntile, tail = rec
-            yield lambda u=u: q_full.try_wait_parity(u & 1)
-            yield lambda n0=n0: slot_full[n0 % K_SLOTS].try_wait_parity((n0 // K_SLOTS) & 1)
+            if not (yield W(lambda u=u: q_full.try_wait_parity(u & 1))):
+                break
+            if not (yield W(lambda n0=n0: slot_full[n0 % K_SLOTS].try_wait_parity((n0 // K_SLOTS) & 1))):
+                break
             if q_buf[0] is None or q_buf[0] != [u, units_per_tile]:
                 log.append(f"S of unit {u} issued on Q buffer {q_buf[0]}")
             for t in range(ntile):
@@ -175,13 +221,18 @@ def simulate(units, rng, plant=None, units_per_tile=2):
                 pipe.append(("commit", q_free))
             pipe.append(("commit", slot_free[n0 % K_SLOTS]))
             yield None
+            live = True
             for j in range(n_kv):
                 nv, nxt, nk = n0 + 2 * j + 1, j + 1 < n_kv, n0 + 2 * j + 2
-                yield lambda nv=nv: slot_full[nv % K_SLOTS].try_wait_parity((nv // K_SLOTS) & 1)
-                if nxt:
-                    yield lambda nk=nk: slot_full[nk % K_SLOTS].try_wait_parity((nk // K_SLOTS) & 1)
+                live = yield W(lambda nv=nv: slot_full[nv % K_SLOTS].try_wait_parity((nv // K_SLOTS) & 1))
+                if live and nxt:
+                    live = yield W(lambda nk=nk: slot_full[nk % K_SLOTS].try_wait_parity((nk // K_SLOTS) & 1))
                 for t in range(ntile):
-                    yield lambda t=t: p_full[t].try_wait_parity(ppar[t])
+                    if not live:
+                        break
+                    live = yield W(lambda t=t: p_full[t].try_wait_parity(ppar[t]))
+                    if not live:
+                        break
                     ppar[t] ^= 1
                     if tail and not nxt and t == 0:
                         st = slot[nv % K_SLOTS]
@@ -195,35 +246,47 @@ def simulate(units, rng, plant=None, units_per_tile=2):
                         q_readers[0] += 1
                         pipe.append(("S", t, u, j + 1, s))
                         pipe.append(("commit", s_full[t]))
+                if not live:
+                    break
                 if j + 2 == n_kv:
                     pipe.append(("commit", q_free))
                 pipe.append(("commit", slot_free[nv % K_SLOTS]))
                 if nxt:
                     pipe.append(("commit", slot_free[nk % K_SLOTS]))
                 yield None
+            if not live:
+                break
             n0 += 2 * n_kv
             unit_empty[u % 2].arrive()
+        if plant == "no_mma_drain":
+            return
+        # every product has completed before tensor memory is released
+        pipe.append(("commit", drain))
+        yield P(lambda: drain.try_wait_parity(0))
 
     def softmax(t):
         n0 = 0
         jpar = 0
         for u in range(total_units + 1):
-            yield lambda u=u: unit_full[u % 2].try_wait_parity((u // 2) & 1)
+            if not (yield W(lambda u=u: unit_full[u % 2].try_wait_parity((u // 2) & 1))):
+                return
             rec = records[u % 2]
             if rec is None:
-                break
+                return
             n_kv, ntile, tail = rec
             if plant == "jpar_per_unit":
                 jpar = 0            # wrong: the barrier's phases run on across units
             if t < ntile:
                 for j in range(n_kv):
-                    yield lambda: s_full[t].try_wait_parity(jpar)
+                    if not (yield W(lambda jp=jpar: s_full[t].try_wait_parity(jp))):
+                        return
                     jpar ^= 1
                     if s_tile[t] != (u, j):
                         log.append(f"head {t} read S {s_tile[t]} as unit {u} tile {j}")
                     if j + 1 == n_kv and tail and t == 0 and plant != "fixer_warp":
                         nv = n0 + 2 * n_kv - 1
-                        yield lambda nv=nv: slot_full[nv % K_SLOTS].try_wait_parity((nv // K_SLOTS) & 1)
+                        if not (yield W(lambda nv=nv: slot_full[nv % K_SLOTS].try_wait_parity((nv // K_SLOTS) & 1))):
+                            return
                         st = slot[nv % K_SLOTS]
                         if st is None or st[0] != nv or st[1] != units_per_tile:
                             log.append(f"V tail of unit {u} zeroed on stage holding {st}")
@@ -231,7 +294,8 @@ def simulate(units, rng, plant=None, units_per_tile=2):
                             st[2] = True
                     p_full[t].arrive()
                     yield None
-                yield lambda: o_done[t].try_wait_parity(jpar ^ 1)
+                if not (yield W(lambda jp=jpar: o_done[t].try_wait_parity(jp ^ 1))):
+                    return
                 if o_count[t] != [u, n_kv]:
                     log.append(f"epilogue of head {t} unit {u} read O after {o_count[t]}")
             n0 += 2 * n_kv
@@ -242,14 +306,16 @@ def simulate(units, rng, plant=None, units_per_tile=2):
         # published, waiting on the stage by parity alone
         n0 = 0
         for u in range(total_units + 1):
-            yield lambda u=u: unit_full[u % 2].try_wait_parity((u // 2) & 1)
+            if not (yield W(lambda u=u: unit_full[u % 2].try_wait_parity((u // 2) & 1))):
+                return
             rec = records[u % 2]
             if rec is None:
-                break
+                return
             n_kv, ntile, tail = rec
             if tail:
                 nv = n0 + 2 * n_kv - 1
-                yield lambda nv=nv: slot_full[nv % K_SLOTS].try_wait_parity((nv // K_SLOTS) & 1)
+                if not (yield W(lambda nv=nv: slot_full[nv % K_SLOTS].try_wait_parity((nv // K_SLOTS) & 1))):
+                    return
                 st = slot[nv % K_SLOTS]
                 if st is None or st[0] != nv or st[1] != units_per_tile:
                     log.append(f"V tail of unit {u} zeroed on stage holding {st}")
@@ -263,9 +329,21 @@ def simulate(units, rng, plant=None, units_per_tile=2):
     waits = [None] * len(procs)
     done = [False] * len(procs)
 
-    def advance(k):
+    def ready(k):
+        w = waits[k]
+        if w is None:
+            return True
+        if isinstance(w, W):
+            return w.pred() or abort[0]
+        return w.pred()
+
+    def advance(k, first=False):
+        w = waits[k]
         try:
-            waits[k] = next(procs[k])
+            if first:
+                waits[k] = next(procs[k])
+            else:
+                waits[k] = procs[k].send(True if w is None else bool(w.pred()))
         except StopIteration:
             done[k] = True
 
@@ -286,17 +364,26 @@ def simulate(units, rng, plant=None, units_per_tile=2):
                 o_count[t][1] += 1
 
     for k in range(len(procs)):
-        advance(k)
-    for _ in range(400000):
+        advance(k, first=True)
+    for step in range(400000):
         if log:
             break
-        ready = [k for k in range(len(procs)) if not done[k] and (waits[k] is None or waits[k]())]
-        choices = [("r", k) for k in ready] + [("c", i) for i in range(len(inflight))]
+        if all(done):
+            # the CTA releases tensor memory and ends
+            if inflight:
+                log.append(f"{len(inflight)} copies still landing when the CTA ends")
+            if pipe:
+                log.append(f"{len(pipe)} tensor-core products or commits still pending when the CTA "
+                           "releases tensor memory")
+            break
+        if step == abort_at:
+            abort[0] = True
+        rdy = [k for k in range(len(procs)) if not done[k] and ready(k)]
+        choices = [("r", k) for k in rdy] + [("c", i) for i in range(len(inflight))]
         if pipe:
             choices.append(("m", 0))
         if not choices:
-            if not all(done):
-                log.append("deadlock: every wait would time out")
+            log.append("deadlock: every wait would time out")
             break
         kind, k = rng.choice(choices)
         if kind == "r":
@@ -314,8 +401,6 @@ def simulate(units, rng, plant=None, units_per_tile=2):
                 if slot[s] is not None and slot[s][0] == n:
                     slot[s][1] += 1
                 slot_full[s].complete_tx(1)
-    if not log and inflight:
-        log.append(f"{len(inflight)} copies still landing when the CTA ends")
     return log
 
 
@@ -327,11 +412,12 @@ def random_units(rng, tails=True):
     return out
 
 
-def run_many(runs, seed, plant=None):
+def run_many(runs, seed, plant=None, aborts=False):
     rng = random.Random(seed)
     bad = []
     for _ in range(runs):
-        log = simulate(random_units(rng), rng, plant)
+        abort_at = rng.randrange(0, 400) if aborts else None
+        log = simulate(random_units(rng), rng, plant, abort_at=abort_at)
         if log:
             bad.append(log[0])
     return bad
@@ -357,3 +443,23 @@ def test_s_parity_restarting_per_unit_is_caught():
 def test_q_reload_without_q_free_races():
     bad = run_many(300, 23, plant="no_q_free_wait")
     assert any("Q of unit" in b or "issued on Q buffer" in b for b in bad), bad[:3]
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_abort_at_any_moment_leaves_cleanly(seed):
+    """The abort flag raised at a random step (some wait of the CTA ran out):
+    every role leaves, nothing deadlocks, the tiles that are still used are
+    the right ones, and when the CTA ends no copy is landing and no product
+    or commit is pending."""
+    bad = run_many(400, 7000 + seed, aborts=True)
+    assert not bad, bad[:3]
+
+
+def test_producer_leaving_without_its_copies_is_caught():
+    bad = run_many(400, 29, plant="no_copy_drain", aborts=True)
+    assert any("copies still landing" in b for b in bad), bad[:3]
+
+
+def test_mma_leaving_without_drain_is_caught():
+    bad = run_many(400, 31, plant="no_mma_drain", aborts=True)
+    assert any("still pending" in b for b in bad), bad[:3]

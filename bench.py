@@ -41,6 +41,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 NOMINAL_HBM_GBS = 7900.0      # HBM3e data-sheet bandwidth of one GB300 (context for the fraction)
 STORE_SETS = 4                 # rotating input sets of the kv_store timing (4 x 160 MB > 129 MB L2)
+# DRAM traffic of one launch of the headline step's split-decode kernel, from
+# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the source
+# whose sha256 starts with the key; reported only while decode.cu still hashes
+# to it (a changed kernel makes the counters stale).
+DECODE_TRAFFIC = {"51f403bd7cd6b9a4": 661777920}
 
 
 def peaks():
@@ -751,8 +756,8 @@ def run_ours(args, rank, world):
         "gpu_launches": dec_launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(dec_achieved, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(dec_achieved / hbm, 4),
-                     # DRAM bytes need ncu, which a timed run does not use
-                     "traffic": None,
+                     "traffic": decode_traffic(),
+                     "traffic_kernel": "decode_split_kernel (ncu capture of the same workload)",
                      "frac_of_nominal": round(dec_achieved / NOMINAL_HBM_GBS, 4),
                      "kernel": "paged_attn_decode_store (split kernel + merge kernel)",
                      "kernel_ms": round(dec_ms, 4),
@@ -768,6 +773,18 @@ def run_ours(args, rank, world):
         "also": also,
     }
     return line
+
+
+def decode_traffic():
+    """DRAM bytes per launch of the split-decode kernel from its ncu capture,
+    or None once decode.cu differs from the captured source."""
+    import hashlib
+    src = Path(__file__).resolve().parent / "paged_kv_cache_303_gb300" / "csrc" / "decode.cu"
+    try:
+        digest = hashlib.sha256(src.read_bytes()).hexdigest()
+    except OSError:
+        return None
+    return DECODE_TRAFFIC.get(digest[:16])
 
 
 def run_reference(args, rank, world):

@@ -47,9 +47,15 @@ def test_decode_store_vs_oracle_and_unfused(shape, chunk_tiles, request):
         ops.set_decode_chunk_tiles(chunk_tiles)
         request.addfinalizer(lambda: ops.set_decode_chunk_tiles(0))
     need = sum((c + bs - 1) // bs for c in ctx) + 3
-    heads = W.Heads(hq, hkv, d, bs, need)
-    work = W.decode_work(heads, ctx, seed=700 + hq + d + bs)
-    kc, vc = W.history_cache(heads, 701 + bs)
+    _decode_store_case(W.Heads(hq, hkv, d, bs, need), ctx, seed=700 + hq + d + bs, cache_seed=701 + bs)
+
+
+def _decode_store_case(heads, ctx, seed, cache_seed):
+    """paged_attn_decode_store against the oracle (outputs, and the cache bit
+    for bit with NaN canaries in the unused slots) and against the unfused
+    four-launch sequence (outputs bit for bit)."""
+    work = W.decode_work(heads, ctx, seed=seed)
+    kc, vc = W.history_cache(heads, cache_seed)
     _poison_unused(kc, vc, work.block_tables, work.context_lens)
     kref, vref = bits(kc).copy(), bits(vc).copy()
     slots = oracle.decode_slots(work.block_tables, work.context_lens, heads.block_size)

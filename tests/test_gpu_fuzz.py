@@ -5,17 +5,29 @@ combinations at random: head shapes with GQA groups 1, 2, 3, 4, 5 and 8,
 head_dim 64 and 128, every power-of-two block size from 1 to 256, length
 mixes that hit the tile edges (0, 1, 63-65, 127-129 rows or keys) beside
 uniform draws, cached prefixes aligned or not to the block size, and decode
-batches with padding rows (context 0).  Unused cache slots hold NaN, so a
-masked key that reached a sum would show.  Every case is fixed by its seed.
+batches with padding rows (context 0), for the decode call and the fused
+store + decode step.  Unused cache slots hold NaN, so a masked key that
+reached a sum would show.  Every case is fixed by its seed.
 """
 import random
 
 import pytest
 
+from paged_kv_cache_303_gb300 import ops
 from paged_kv_cache_303_gb300 import workloads as W
+from test_gpu_fused import _decode_store_case
 from test_gpu_parity import _decode_case, _prefill_packed, _prefill_paged
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_303_gb300 import build
+    build.build()
+    ops.device_status(clear=True)
+    yield
+    assert ops.device_status(clear=True) == 0, "a kernel flagged its input"
 
 # (query heads, kv heads): groups 1, 2, 3, 4, 5, 8
 HEAD_SHAPES = [(8, 8), (16, 8), (12, 4), (10, 2), (16, 4), (32, 4), (5, 1)]
@@ -61,13 +73,24 @@ def test_random_paged_prefill(seed):
     _prefill_paged(heads, q_lens, prefix, seed=23000 + seed, growing=rng.random() < 0.3)
 
 
-@pytest.mark.parametrize("seed", range(27))
-def test_random_decode(seed):
-    rng = random.Random(24000 + seed)
+def _decode_draw(rng: random.Random, seed: int):
     bs = BLOCK_SIZES[seed % len(BLOCK_SIZES)]
     ctx = [rng.choice([0, 1, bs, bs + 1]) if rng.random() < 0.3 else _length(rng, 3000)
            for _ in range(rng.randint(1, 9))]
     if not any(ctx):
         ctx[0] = 1
-    heads = _heads(rng, bs, ctx, decode=True)
+    return _heads(rng, bs, ctx, decode=True), ctx
+
+
+@pytest.mark.parametrize("seed", range(27))
+def test_random_decode(seed):
+    heads, ctx = _decode_draw(random.Random(24000 + seed), seed)
     _decode_case(heads, ctx, seed=25000 + seed)
+
+
+@pytest.mark.parametrize("seed", range(27))
+def test_random_decode_store(seed):
+    """The fused step (decode slot, K/V store and decode in one launch):
+    oracle, cache bits and the unfused sequence."""
+    heads, ctx = _decode_draw(random.Random(26000 + seed), seed)
+    _decode_store_case(heads, ctx, seed=27000 + seed, cache_seed=28000 + seed)

@@ -681,6 +681,58 @@ def test_decode_step_replayed_as_cuda_graph():
     assert got[1].eq(0).all()
 
 
+def test_prefill_step_replayed_as_cuda_graph():
+    """A prefix-cache step (slot mapping, K/V store, paged prefill: planning
+    kernel and prefill kernel, the latter a programmatic dependent) captured
+    once in a CUDA graph and replayed twice on new chunks; each replay's
+    output against the oracle.  The work list and the claim counter are
+    rebuilt by every replay's planning kernel."""
+    heads = W.Heads(16, 8, 128, 64, 160)
+    q_lens, prefix = [300, 77, 129, 1], [128, 5, 0, 640]
+    work = W.prefill_work(heads, q_lens, prefix, seed=970)
+    kc, vc = W.history_cache(heads, 971)
+    gk, gv = dev(kc), dev(vc)
+    q, k, v = dev(work.q), dev(work.k), dev(work.v)
+    bt, start = dev(work.block_tables), dev(work.prefix_lens)
+    cu_q, cu_k = dev(work.cu_seqlens_q), dev(work.cu_seqlens_k)
+    slots = torch.empty(work.total_q, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    ws = torch.empty(ops.prefill_workspace_size(len(q_lens), work.total_q, work.max_seqlen_q, 16),
+                     dtype=torch.uint8, device="cuda")
+
+    def step():
+        ops.kv_build_slot_mapping(bt, start, cu_q, heads.block_size, out=slots)
+        ops.kv_store(k, v, gk, gv, slots)
+        ops.paged_attn_prefill(q, None, None, cu_q, cu_k, work.max_seqlen_q, work.max_seqlen_k,
+                               heads.scale, k_cache=gk, v_cache=gv, block_tables=bt, out=out,
+                               workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    kref, vref = bits(kc).copy(), bits(vc).copy()
+    ref_slots = oracle.slot_mapping(work.block_tables, work.prefix_lens, work.cu_seqlens_q, 64)
+    for rep in range(2):
+        g = W.generator(980 + rep)
+        nq, nk, nv = (W.normal_bf16(tuple(t.shape), g) for t in (work.q, work.k, work.v))
+        q.copy_(nq.cuda())
+        k.copy_(nk.cuda())
+        v.copy_(nv.cuda())
+        graph.replay()
+        torch.cuda.synchronize()
+        oracle.kv_store(bits(nk), bits(nv), kref, vref, ref_slots)
+        ref, _ = oracle.prefill(bits(nq), None, None, work.cu_seqlens_q, work.cu_seqlens_k,
+                                heads.scale, k_cache=kref, v_cache=vref,
+                                block_tables=work.block_tables)
+        assert_close(out, ref, f"prefill graph replay {rep}")
+    assert np.array_equal(bits(gk), kref) and np.array_equal(bits(gv), vref)
+
+
 def test_mixed_batch_chunks_and_decode_rows_in_one_prefill():
     """Chunked-prefill mixed batch: sequences with a cached prefix and a new
     chunk, and decode rows (one new token over their whole cache), run as one

@@ -262,3 +262,41 @@ def test_pipelined_end_to_end_steps_read_back_the_decode_output():
         assert torch.equal(oh, st.out.cpu())
     tw = st.twin()
     assert tw.kc.data_ptr() == st.kc.data_ptr() and tw.inputs.data_ptr() != st.inputs.data_ptr()
+
+
+def test_prefill_and_decode_store_on_two_streams_at_once():
+    """A packed prefill and a fused decode step launched on two streams,
+    where they can run at the same time, three rounds: when both persistent
+    grids share the SMs, each claims only its own work, and both outputs
+    match the oracle."""
+    from paged_kv_cache_303_gb300 import workloads as W
+    ph = W.Heads(16, 8, 128, 16, 256)
+    pw = W.prefill_work(ph, [700, 129, 64, 1000], seed=990)
+    pref, _ = oracle.prefill(bits(pw.q), bits(pw.k), bits(pw.v), pw.cu_seqlens_q, pw.cu_seqlens_k,
+                             ph.scale)
+    dh = W.Heads(16, 8, 128, 64, 256)
+    dw = W.decode_work(dh, [3000, 1, 0, 2000, 777, 4000], seed=991)
+    kc, vc = W.history_cache(dh, 992)
+    kref, vref = bits(kc).copy(), bits(vc).copy()
+    dslots = oracle.decode_slots(dw.block_tables, dw.context_lens, dh.block_size)
+    oracle.kv_store(bits(dw.k), bits(dw.v), kref, vref, dslots)
+    dref, _ = oracle.decode(bits(dw.q), kref, vref, dw.block_tables, dw.context_lens, dh.scale,
+                            nthreads=0)
+    pq, pk, pv = dev(pw.q), dev(pw.k), dev(pw.v)
+    cu_q, cu_k = dev(pw.cu_seqlens_q), dev(pw.cu_seqlens_k)
+    dq, dk, dv = dev(dw.q), dev(dw.k), dev(dw.v)
+    bt, ctx = dev(dw.block_tables), dev(dw.context_lens)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        gk, gv = dev(kc), dev(vc)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s1):
+            pout = ops.paged_attn_prefill(pq, pk, pv, cu_q, cu_k, pw.max_seqlen_q, pw.max_seqlen_k,
+                                          ph.scale)
+        with torch.cuda.stream(s2):
+            dout = ops.paged_attn_decode_store(dq, dk, dv, gk, gv, bt, ctx, dw.max_context_len,
+                                               dh.scale)
+        torch.cuda.synchronize()
+        assert_close(pout, pref, "prefill beside a decode")
+        assert_close(dout, dref, "decode beside a prefill")
+        assert np.array_equal(bits(gk), kref) and np.array_equal(bits(gv), vref)

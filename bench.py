@@ -346,13 +346,46 @@ class PrefillStep:
             ev[1].record()
 
 
+def time_graph_launches(launch, per_graph: int, steps: int, warmup: int, world: int):
+    """Median time of one launch of `launch(i)` with no host in the loop: the
+    launches i = 0 .. per_graph-1 are captured once as a CUDA graph, and each
+    of `steps` replays is timed with CUDA events; a launch's time is the
+    replay's over per_graph.  (Events around each eager call would also time
+    the host's own per-call work whenever a launch is shorter than it.)"""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(per_graph):
+            launch(i)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(per_graph):
+            launch(i)
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        evs[i][0].record()
+        graph.replay()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return statistics.median(a.elapsed_time(b) for a, b in evs) / per_graph
+
+
 def time_store_rotating(pre, steps: int, warmup: int, world: int):
     """kv_store of the prefill step's tokens, timed alone over STORE_SETS
     rotating sets of inputs: copies of the new k/v rows, each with its own
     slots in disjoint cache blocks.  A launch reads rows and writes cache
-    lines that the other sets' launches (3 x 160 MB since) have pushed out of
-    L2, and makes room by writing back their dirty lines: the steady state
-    of a stream of stores.  Returns the median launch time in ms."""
+    lines that the other sets' launches have pushed out of L2, and makes room
+    by writing back their dirty lines: the steady state of a stream of
+    stores.  The sets' launches run in turn from a CUDA graph.  Returns the
+    median launch time in ms."""
     from paged_kv_cache_303_gb300 import workloads as W
     w, h = pre.work, pre.work.heads
     n, bs = w.total_q, h.block_size
@@ -364,22 +397,31 @@ def time_store_rotating(pre, steps: int, warmup: int, world: int):
         blocks = perm[r * nb:(r + 1) * nb].to(torch.int64)
         slots = (blocks[:, None] * bs + torch.arange(bs)[None, :]).reshape(-1)[:n]
         sets.append((pre.k.clone(), pre.v.clone(), slots.to(torch.int32).cuda()))
-    for i in range(warmup):
+
+    def launch(i):
         k, v, sl = sets[i % STORE_SETS]
         pre.ops.kv_store(k, v, pre.kc, pre.vc, sl)
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    for i in range(steps):
-        k, v, sl = sets[i % STORE_SETS]
-        evs[i][0].record()
-        pre.ops.kv_store(k, v, pre.kc, pre.vc, sl)
-        evs[i][1].record()
-    torch.cuda.synchronize()
-    barrier(world)
-    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    return time_graph_launches(launch, STORE_SETS, steps, warmup, world)
+
+
+def back_to_back(flops, ms, tfl):
+    """The prefill call's rate when calls follow one another with no idle
+    stream before them (four calls per CUDA graph): the single-call figure
+    also holds the first kernel's launch latency on an idle stream."""
+    return {"tflops": round(flops / (ms / 1e3) / 1e12, 2), "kernel_ms": round(ms, 4),
+            "frac": round(flops / (ms / 1e3) / 1e12 / tfl, 4),
+            "timing": "four calls captured in one CUDA graph, replay time / 4"}
+
+
+def time_decode_store(dec, steps: int, warmup: int, world: int):
+    """kv_store of a decode step's new rows (one per sequence, -1 for padding
+    rows) timed alone: a few hundred KB, so each launch is timed from a CUDA
+    graph of 8 launches.  Returns the median launch time in ms."""
+    h = dec.work.heads
+    dec.ops.kv_build_decode_slots(dec.bt, dec.ctx, h.block_size, out=dec.slots)
+    return time_graph_launches(lambda i: dec.ops.kv_store(dec.k, dec.v, dec.kc, dec.vc, dec.slots),
+                               8, steps, warmup, world)
 
 
 def time_steps(step, steps: int, warmup: int, world: int, kernel_events=True):
@@ -521,6 +563,7 @@ def section_prefill_varlen(args, world, hbm, tfl):
     out = {}
     pre = PrefillStep(W.varlen_prefill(), cache_seed=501)
     tot, pre_ms, _ = time_steps(pre, args.steps, args.warmup, world)
+    b2b_ms = time_graph_launches(lambda i: pre.attention(), 4, args.steps, args.warmup, world)
     st_ms = time_store_rotating(pre, args.steps, args.warmup, world)
     out["prefill_varlen"] = {
         "workload": "varlen-prefill-8x: 8 prompts U[128,4096] (%d tokens), 16q/8kv/128d" % pre.work.total_q,
@@ -529,12 +572,14 @@ def section_prefill_varlen(args, world, hbm, tfl):
         "roofline": {"bound": "tensor", "peak": tfl, "unit": "TFLOP/s",
                      "frac": round(pre.flops / (pre_ms / 1e3) / 1e12 / tfl, 4)},
         "flops_per_launch": pre.flops,
+        "back_to_back": back_to_back(pre.flops, b2b_ms, tfl),
     }
     out["prefill_varlen"]["l2"] = "no flush: the prefill reads q, k, v (160 MB, more than the 129 MB L2)"
     out["kv_store"] = {
         "workload": "store of the varlen-prefill step's %d tokens (D=1024)" % pre.work.total_q,
         "l2": ("inputs larger than L2: the store is timed alone over %d rotating sets of new k/v rows, "
-               "each with its own cache slots (%d x 160 MB per round)" % (STORE_SETS, STORE_SETS)),
+               "each with its own cache slots (%d x 160 MB per round), launched in turn from a CUDA "
+               "graph" % (STORE_SETS, STORE_SETS)),
         "gbs": round(pre.store_bytes / (st_ms / 1e3) / 1e9, 1), "kernel_ms": round(st_ms, 4),
         "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
                      "frac": round(pre.store_bytes / (st_ms / 1e3) / 1e9 / hbm, 4)},
@@ -563,20 +608,32 @@ def section_prologue(args, world, hbm):
     return out
 
 
-def section_prefill_prefix(args, world, tfl):
+def section_prefill_prefix(args, world, hbm, tfl):
     """Prefix-cache prefill: cached prefixes read through block_tables."""
     from paged_kv_cache_303_gb300 import workloads as W
     pp = PrefillStep(W.prefix_prefill(), cache_seed=601)
     tot, pp_ms, _ = time_steps(pp, args.steps, args.warmup, world)
-    out = {"prefill_prefix": {
+    b2b_ms = time_graph_launches(lambda i: pp.attention(), 4, args.steps, args.warmup, world)
+    st_ms = time_store_rotating(pp, args.steps, args.warmup, world)
+    out = {"kv_store_prefix": {
+        "workload": "store of the prefix-prefill step's %d new tokens (D=1024)" % pp.work.total_q,
+        "l2": ("inputs larger than L2: timed alone over %d rotating sets of new k/v rows, each with "
+               "its own cache slots, launched in turn from a CUDA graph" % STORE_SETS),
+        "gbs": round(pp.store_bytes / (st_ms / 1e3) / 1e9, 1), "kernel_ms": round(st_ms, 4),
+        "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                     "frac": round(pp.store_bytes / (st_ms / 1e3) / 1e9 / hbm, 4)},
+        "bytes_per_launch": pp.store_bytes,
+    }}
+    out["prefill_prefix"] = {
         "workload": "prefix-prefill-16x: prefix U{0..12}x256 + chunk U[64,1024] (%d new tokens)" % pp.work.total_q,
         "tflops": round(pp.flops / (pp_ms / 1e3) / 1e12, 2), "kernel_ms": round(pp_ms, 4),
         "roofline": {"bound": "tensor", "peak": tfl, "unit": "TFLOP/s",
                      "frac": round(pp.flops / (pp_ms / 1e3) / 1e12 / tfl, 4)},
         "flops_per_launch": pp.flops,
+        "back_to_back": back_to_back(pp.flops, b2b_ms, tfl),
         "l2": ("no flush: the prefill reads the cached prefixes and the chunk through block_tables "
                "(about 139 MB of K/V) and q, more than the 129 MB L2"),
-    }}
+    }
     del pp
     torch.cuda.empty_cache()
     return out
@@ -590,11 +647,15 @@ def section_decode_large(args, world, hbm):
     pads = batch // 8
     big = DecodeStep(W.large_decode(batch=batch, pads=pads, num_blocks=pool), cache_seed=701)
     tot, big_ms, _ = time_steps(big, args.steps, args.warmup, world)
+    bs_ms = time_decode_store(big, args.steps, args.warmup, world)
     out = {"decode_large": {
         "workload": f"large-decode-b{batch}p{pads}: 32q/8kv/128d, {batch}+{pads} pad rows, "
                     f"lognormal ctx [1k,32k], {pool}-block pool",
         "gbs": round(big.bytes / (big_ms / 1e3) / 1e9, 1), "kernel_ms": round(big_ms, 4),
         "step_gbs": round(big.bytes / (tot / args.steps / 1e3) / 1e9, 1),
+        "store_us": round(bs_ms * 1e3, 2),
+        "store_note": f"kv_store of the step's {batch + pads} rows ({pads} padding rows skipped) "
+                      "timed alone from a CUDA graph of 8 launches",
         "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
                      "frac": round(big.bytes / (big_ms / 1e3) / 1e9 / hbm, 4)},
         "bytes_per_launch": big.bytes,
@@ -632,7 +693,7 @@ def run_only(args, rank, world):
     fn = {"decode": lambda: section_decode(args, world, hbm),
           "prefill_varlen": lambda: section_prefill_varlen(args, world, hbm, tfl),
           "qk_norm_rope_store": lambda: section_prologue(args, world, hbm),
-          "prefill_prefix": lambda: section_prefill_prefix(args, world, tfl),
+          "prefill_prefix": lambda: section_prefill_prefix(args, world, hbm, tfl),
           "decode_large": lambda: section_decode_large(args, world, hbm)}[args.only]
     return {"metric": METRIC, "only": args.only, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "also": fn()}
@@ -715,11 +776,17 @@ def run_ours(args, rank, world):
                      "frac": round(u_bytes / (u_ms / 1e3) / 1e9 / hbm, 4)},
         "launches_per_step": uf.launches,
     }
+    ds_ms = time_decode_store(uf, args.steps, args.warmup, world)
+    also["kv_store_decode"] = {
+        "workload": "store of the qwen3-decode-b64 step's 64 new rows (%d bytes)" % uf.store_bytes,
+        "us": round(ds_ms * 1e3, 2),
+        "note": "a few hundred KB per launch: microseconds, timed from a CUDA graph of 8 launches",
+    }
     del uf, ugraph
     torch.cuda.empty_cache()
     also.update(section_prefill_varlen(args, world, hbm, tfl))
     also.update(section_prologue(args, world, hbm))
-    also.update(section_prefill_prefix(args, world, tfl))
+    also.update(section_prefill_prefix(args, world, hbm, tfl))
     if not args.skip_large:
         also.update(section_decode_large(args, world, hbm))
 

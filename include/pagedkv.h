@@ -267,8 +267,10 @@ size_t paged_attn_prefill_workspace_size(int32_t num_seqs, int32_t total_q,
  * which the kernel's resident CTAs claim chunks, zeroed by the call in stream
  * order, and the chunk partials); content need not be initialised.  Calls
  * that share a workspace must be ordered on the device.
- * Supported: head_dim 64 or 128; num_heads / num_kv_heads from 1 to 8;
- * block_size a power of two.
+ * Supported: head_dim 64 or 128; any num_heads / num_kv_heads; block_size a
+ * power of two.  A GQA group of G > 8 query heads runs as r sub-groups of
+ * G / r heads (r the smallest divisor of G with G / r <= 8), each reading
+ * the group's keys and values: such a call reads them r times.
  * ---------------------------------------------------------------------- */
 int paged_attn_decode(const pkv_bf16 *q, int64_t q_row_stride,
                       const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, int64_t num_blocks,
@@ -286,7 +288,9 @@ size_t paged_attn_decode_workspace_size(int32_t batch, int32_t num_heads,
 /* ------------------------------------------------------------------------
  * paged_attn_decode_store -- the write-then-attend order of Lesson 04 §4
  * (store_kvcache, then flash_attn_with_kvcache) and the decode slot of
- * §4/L17 §5.3, in one launch.
+ * §4/L17 §5.3, in one launch (for a GQA group of more than 8 query heads,
+ * whose sub-groups read each kv head from several CTAs, the rows are stored
+ * by a launch of their own just before the decode).
  *
  * For every row b with context_lens[b] >= 1 it writes key[b] and value[b]
  * ([num_kv_heads, head_dim] each) to the decode slot of position

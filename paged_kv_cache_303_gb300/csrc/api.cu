@@ -327,8 +327,8 @@ static int decode_entry(const char *what, const pkv_bf16 *q, int64_t q_row_strid
     if (block_size & (block_size - 1))
         return fail(PKV_ERR_UNSUPPORTED, "%s: block_size must be a power of two", what);
     const int G = num_heads / num_kv_heads;
-    if (G < 1 || G > 8)
-        return fail(PKV_ERR_UNSUPPORTED, "%s: num_heads / num_kv_heads must be 1 to 8", what);
+    if (G < 1)
+        return fail(PKV_ERR_INVALID_ARG, "%s: num_heads / num_kv_heads must be at least 1", what);
     if (!q || !k_cache || !v_cache || !context_lens || !out || (max_blocks_per_seq > 0 && !block_tables))
         return fail(PKV_ERR_INVALID_ARG, "%s: null pointer", what);
     const int64_t row = (int64_t)num_heads * head_dim;

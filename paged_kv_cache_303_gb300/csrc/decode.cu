@@ -164,6 +164,10 @@ struct DecodeParams {
     const uint16_t *new_k, *new_v;
     int64_t new_k_rs, new_v_rs;
     uint16_t *k_cache, *v_cache;
+    // a GQA group larger than the kernel's 8 rows runs as kv_rep sub-groups
+    // of G / kv_rep heads: work items name a virtual kv head v (num_kv_heads *
+    // kv_rep of them) whose keys and values are those of kv head v / kv_rep
+    int32_t kv_rep, num_vheads;   // num_vheads = num_kv_heads * kv_rep
 };
 
 template <bool SW>
@@ -270,7 +274,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 constexpr int kQ = 2;                               // item queue entries
 
 struct ItemRec {
-    int b, kvh, split, tok_begin, tok_end, ntiles, pad0, pad1;
+    int b, kvh, split, tok_begin, tok_end, ntiles, kv, pad1;   // kv: the kv head whose K/V are read
 };
 
 template <int HD, int G>
@@ -320,7 +324,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     const bool direct = (p.max_splits == 1);
     const int bs = p.block_size;
     const int TB = bs < kTile ? bs : kTile;          // slots per TMA box
-    const int per_split = p.batch * p.num_kv_heads;
+    const int per_split = p.batch * p.num_vheads;
     const int total = per_split * p.max_splits;
 
     if (warp == kConsumers && lane == 0) {
@@ -358,8 +362,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             if (have) {
                 it.split = idx / per_split;
                 const int rem = idx % per_split;
-                it.b = rem / p.num_kv_heads;
-                it.kvh = rem % p.num_kv_heads;
+                it.b = rem / p.num_vheads;
+                it.kvh = rem % p.num_vheads;
+                it.kv = it.kvh / p.kv_rep;
                 int ctx = p.ctx[it.b];
                 if (ctx < 0 || ctx > p.max_context_len) {
                     if (lane == 0 && it.split == 0 && it.kvh == 0)
@@ -390,6 +395,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     const int32_t *bt_row = p.bt + (int64_t)it.b * p.bt_stride;
                     const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
                     if (blk >= 0 && blk < p.num_blocks) {
+                        // (the host stores the rows in a launch of their own when
+                        // kv_rep > 1, so that every sub-group's reads see them)
                         const int64_t dst = ((int64_t)blk * bs + pos % bs) * p.num_kv_heads * HD +
                                             (int64_t)it.kvh * HD + lane * DPL;
                         const uint16_t *ks = p.new_k + (int64_t)it.b * p.new_k_rs + (int64_t)it.kvh * HD + lane * DPL;
@@ -471,8 +478,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
                         for (int hf = 0; hf < L::kHalves; ++hf) {
                             const int off = hf * kTile * 128 + sg * TB * 128;
-                            tma_load_3d(kdst + off, &kmap, &full[stage], hf * 64, it.kvh, z, policy);
-                            tma_load_3d(vdst + off, &vmap, &full[stage], hf * 64, it.kvh, z, policy);
+                            tma_load_3d(kdst + off, &kmap, &full[stage], hf * 64, it.kv, z, policy);
+                            tma_load_3d(vdst + off, &vmap, &full[stage], hf * 64, it.kv, z, policy);
                         }
                     }
                 }
@@ -764,6 +771,31 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
     merge_head<HD>(p, b, hq, (ctx + p.chunk - 1) / p.chunk, lane);
 }
 
+// The new K/V rows of a decode step written on their own (a GQA group split
+// into sub-groups reads each kv head from several CTAs, which must all see
+// the row): one warp per (row, kv head), the slot of position ctx - 1.
+template <int HD>
+__global__ void __launch_bounds__(128) decode_store_rows_kernel(const DecodeParams p) {
+    constexpr int DPL = HD / 32;
+    const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (w >= p.batch * p.num_kv_heads) return;
+    const int b = w / p.num_kv_heads, kvh = w % p.num_kv_heads;
+    const int ctx = p.ctx[b];
+    if (ctx <= 0 || ctx > p.max_context_len) return;      // padding row, or flagged by the decode
+    const int pos = ctx - 1, bs = p.block_size, lb = pos / bs;
+    const int32_t *bt_row = p.bt + (int64_t)b * p.bt_stride;
+    const int blk = lb < p.max_blocks ? bt_row[lb] : -1;
+    if (blk < 0 || blk >= p.num_blocks) return;             // flagged by the decode's loads
+    const int64_t dst = ((int64_t)blk * bs + pos % bs) * p.num_kv_heads * HD + (int64_t)kvh * HD + lane * DPL;
+    const uint16_t *ks = p.new_k + (int64_t)b * p.new_k_rs + (int64_t)kvh * HD + lane * DPL;
+    const uint16_t *vs = p.new_v + (int64_t)b * p.new_v_rs + (int64_t)kvh * HD + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) {
+        p.k_cache[dst + i] = ks[i];
+        p.v_cache[dst + i] = vs[i];
+    }
+}
+
 template <int HD, int G, bool SW>
 int launch_split(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &p, int batch,
                  int num_kv_heads, cudaStream_t stream, const char **err) {
@@ -806,13 +838,20 @@ int dispatch_group(int G, const CUtensorMap &km, const CUtensorMap &vm, const De
         case 6: return launch_split<HD, 6, SW>(km, vm, p, batch, hkv, s, err);
         case 7: return launch_split<HD, 7, SW>(km, vm, p, batch, hkv, s, err);
         case 8: return launch_split<HD, 8, SW>(km, vm, p, batch, hkv, s, err);
-        default: *err = "num_heads / num_kv_heads must be 1 to 8"; return PKV_ERR_UNSUPPORTED;
+        default: *err = "GQA sub-group of more than 8 heads"; return PKV_ERR_UNSUPPORTED;
     }
 }
 
 }  // namespace
 
 std::atomic<int> g_decode_chunk_tiles{0};
+
+int decode_kv_rep(int32_t num_heads, int32_t num_kv_heads) {
+    const int G = num_heads / num_kv_heads;
+    int r = 1;
+    while (G / r > 8 || G % r != 0) ++r;
+    return r;
+}
 
 void decode_plan(int32_t batch, int32_t num_kv_heads, int32_t head_dim, int32_t max_context_len,
                  int32_t *chunk, int32_t *max_splits) {
@@ -843,7 +882,8 @@ void decode_plan(int32_t batch, int32_t num_kv_heads, int32_t head_dim, int32_t 
 size_t decode_workspace_bytes(int32_t batch, int32_t num_heads, int32_t num_kv_heads,
                               int32_t head_dim, int32_t max_context_len) {
     int32_t chunk, splits;
-    decode_plan(batch, num_kv_heads, head_dim, max_context_len, &chunk, &splits);
+    decode_plan(batch, num_kv_heads * decode_kv_rep(num_heads, num_kv_heads), head_dim, max_context_len,
+                &chunk, &splits);
     // a work counter (256 bytes, first), then the chunk partials
     const size_t counter = 256;
     if (splits <= 1) return counter;
@@ -857,8 +897,9 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream, const char **err) {
         *err = "paged_attn_decode supports head_dim 64 and 128";
         return PKV_ERR_UNSUPPORTED;
     }
+    const int rep = decode_kv_rep(a.num_heads, a.num_kv_heads);
     int32_t chunk, splits;
-    decode_plan(a.batch, a.num_kv_heads, a.head_dim, a.max_context_len, &chunk, &splits);
+    decode_plan(a.batch, a.num_kv_heads * rep, a.head_dim, a.max_context_len, &chunk, &splits);
     DecodeParams p{};
     p.q = a.q;
     p.q_rs = a.q_rs;
@@ -884,6 +925,8 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream, const char **err) {
     p.k_cache = const_cast<uint16_t *>(a.k_cache);
     p.v_cache = const_cast<uint16_t *>(a.v_cache);
     p.batch = a.batch;
+    p.kv_rep = rep;
+    p.num_vheads = a.num_kv_heads * rep;
     // workspace: the item counter (zeroed here, in stream order), then the
     // chunk partials when there is more than one chunk
     const size_t need = decode_workspace_bytes(a.batch, a.num_heads, a.num_kv_heads, a.head_dim,
@@ -911,13 +954,25 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream, const char **err) {
     rc = encode_rows_heads_map(&vm, a.v_cache, num_slots, a.num_kv_heads, a.head_dim,
                                (int64_t)a.num_kv_heads * a.head_dim, a.head_dim, 64, tb, sw, err);
     if (rc) return rc;
-    const int G = a.num_heads / a.num_kv_heads;
+    if (rep > 1 && p.new_k != nullptr) {
+        // the step's rows first, then the decode without its fused store
+        const int warps = a.batch * a.num_kv_heads;
+        if (a.head_dim == 128)
+            decode_store_rows_kernel<128><<<(warps + 3) / 4, 128, 0, stream>>>(p);
+        else
+            decode_store_rows_kernel<64><<<(warps + 3) / 4, 128, 0, stream>>>(p);
+        cudaError_t se = cudaGetLastError();
+        if (se != cudaSuccess) { *err = cudaGetErrorString(se); return PKV_ERR_CUDA; }
+        p.new_k = p.new_v = nullptr;
+    }
+    const int G = a.num_heads / a.num_kv_heads / rep;        // heads per (sub-)group
+    const int nvh = a.num_kv_heads * rep;
     if (a.head_dim == 128)
-        rc = sw ? dispatch_group<128, true>(G, km, vm, p, a.batch, a.num_kv_heads, stream, err)
-                : dispatch_group<128, false>(G, km, vm, p, a.batch, a.num_kv_heads, stream, err);
+        rc = sw ? dispatch_group<128, true>(G, km, vm, p, a.batch, nvh, stream, err)
+                : dispatch_group<128, false>(G, km, vm, p, a.batch, nvh, stream, err);
     else
-        rc = sw ? dispatch_group<64, true>(G, km, vm, p, a.batch, a.num_kv_heads, stream, err)
-                : dispatch_group<64, false>(G, km, vm, p, a.batch, a.num_kv_heads, stream, err);
+        rc = sw ? dispatch_group<64, true>(G, km, vm, p, a.batch, nvh, stream, err)
+                : dispatch_group<64, false>(G, km, vm, p, a.batch, nvh, stream, err);
     if (rc) return rc;
     if (splits > 1) {
         cudaLaunchConfig_t cfg = {};

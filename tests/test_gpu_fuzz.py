@@ -1,7 +1,7 @@
 """Seeded random cases for the attention paths, each against the oracle.
 
 The hand-picked parity cases pin one mechanism each; these draw the
-combinations at random: head shapes with GQA groups 1 to 8,
+combinations at random: head shapes with GQA groups 1 to 8, 12 and 16,
 head_dim 64 and 128, every power-of-two block size from 1 to 256, length
 mixes that hit the tile edges (0, 1, 63-65, 127-129 rows or keys) beside
 uniform draws, cached prefixes aligned or not to the block size, and decode
@@ -29,8 +29,9 @@ def _built():
     yield
     assert ops.device_status(clear=True) == 0, "a kernel flagged its input"
 
-# (query heads, kv heads): groups 1 to 8
-HEAD_SHAPES = [(8, 8), (16, 8), (12, 4), (10, 2), (16, 4), (32, 4), (5, 1), (12, 2), (7, 1)]
+# (query heads, kv heads): groups 1 to 8, 12 and 16
+HEAD_SHAPES = [(8, 8), (16, 8), (12, 4), (10, 2), (16, 4), (32, 4), (5, 1), (12, 2), (7, 1), (24, 2),
+               (32, 2)]
 BLOCK_SIZES = [1, 2, 4, 8, 16, 32, 64, 128, 256]
 EDGE_LENGTHS = [0, 1, 63, 64, 65, 127, 128, 129]
 

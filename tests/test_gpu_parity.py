@@ -218,6 +218,11 @@ DECODE_SHAPES = [
     (10, 2, 64, 16, [90, 333, 0]),
     (12, 2, 128, 32, [64, 1025]),
     (14, 2, 128, 256, [513, 7]),
+    # groups above 8, run as sub-groups of 6, 8, 3 and 1 heads (12, 16, 9, 11)
+    (24, 2, 128, 16, [300, 0, 1000, 1]),
+    (32, 2, 64, 64, [257, 2000]),
+    (9, 1, 128, 8, [100, 33]),
+    (11, 1, 64, 256, [700, 0, 5]),
 ]
 
 

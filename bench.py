@@ -8,7 +8,8 @@ One step = one pass of the hot path over one synthetic batch:
   paged_attn_decode (split-K kernel + merge kernel).
 The headline value is the decode KV-read bandwidth of the whole step
 (sum_b ctx_b * Hkv * d * 2 bytes * 2 tensors / step time).  The prefill
-TFLOP/s (varlen and prefix-cache), the store_kvcache GB/s, and the large
+TFLOP/s (varlen and prefix-cache), the store_kvcache GB/s, a chunked-prefill
+mixed batch (decode rows and prompt chunks in one prefill call) and the large
 padded decode are measured in the same run and reported under "also".
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -643,6 +644,84 @@ def section_prefill_prefix(args, world, hbm, tfl):
     return out
 
 
+def section_prefill_mixed(args, world, hbm, tfl):
+    """Chunked-prefill mixed batch: decode rows and prompt chunks in one paged
+    prefill call, beside the same work as two calls on the same cache (the
+    chunks through paged_attn_prefill, the decode rows through
+    paged_attn_decode).  With 64 decode rows in a 2048-token budget the
+    K/V read dominates, so the roofline is the larger of the bytes' time at
+    the HBM peak and the causal FLOPs' time at the bf16 peak."""
+    from paged_kv_cache_303_gb300 import workloads as W
+    mix = PrefillStep(W.mixed_chunked(), cache_seed=801)
+    w, h, ops = mix.work, mix.work.heads, mix.ops
+    _, one_ms, _ = time_steps(mix, args.steps, args.warmup, world)
+    b2b_ms = time_graph_launches(lambda i: mix.attention(), 4, args.steps, args.warmup, world)
+
+    # the same work as two calls: the decode rows lead the batch
+    q_lens = w.q_lens.tolist()
+    nd = next(i for i, n in enumerate(q_lens) if n != 1)
+    d_ctx = (w.prefix_lens[:nd] + 1).to(torch.int32).cuda()
+    d_max = int(d_ctx.max())
+    d_bt = mix.bt[:nd].contiguous()
+    d_out = torch.empty_like(mix.q[:nd])
+    d_ws = torch.empty(max(ops.decode_workspace_size(nd, h.num_heads, h.num_kv_heads, h.head_dim,
+                                                     d_max), 1), dtype=torch.uint8, device="cuda")
+    c_q = mix.q[nd:]
+    c_cu_q = (w.cu_seqlens_q[nd:] - w.cu_seqlens_q[nd]).cuda()
+    c_cu_k = (w.cu_seqlens_k[nd:] - w.cu_seqlens_k[nd]).cuda()
+    c_bt = mix.bt[nd:].contiguous()
+    c_max_q = max(q_lens[nd:])
+    c_max_k = int((w.q_lens[nd:] + w.prefix_lens[nd:]).max())
+    c_out = torch.empty_like(c_q)
+    c_ws = torch.empty(max(ops.prefill_workspace_size(len(q_lens) - nd, c_q.shape[0], c_max_q,
+                                                      h.num_heads), 1),
+                       dtype=torch.uint8, device="cuda")
+
+    def two_calls(i):
+        ops.paged_attn_prefill(c_q, None, None, c_cu_q, c_cu_k, c_max_q, c_max_k, h.scale,
+                               k_cache=mix.kc, v_cache=mix.vc, block_tables=c_bt, out=c_out,
+                               workspace=c_ws)
+        ops.paged_attn_decode(mix.q[:nd], mix.kc, mix.vc, d_bt, d_ctx, d_max, h.scale, out=d_out,
+                              workspace=d_ws)
+
+    two_ms = time_graph_launches(two_calls, 4, args.steps, args.warmup, world)
+
+    keys = int((w.q_lens + w.prefix_lens).to(torch.int64).sum())
+    nbytes = keys * h.num_kv_heads * h.head_dim * 2 * 2 + 2 * w.total_q * h.num_heads * h.head_dim * 2
+    flops = mix.flops
+    hbm_bound = nbytes / hbm / 1e9 >= flops / tfl / 1e12
+
+    def rates(ms):
+        gbs, tf = nbytes / (ms / 1e3) / 1e9, flops / (ms / 1e3) / 1e12
+        return round(gbs, 1), round(tf, 2), round(gbs / hbm if hbm_bound else tf / tfl, 4)
+
+    gbs, tf, frac = rates(one_ms)
+    b_gbs, b_tf, b_frac = rates(b2b_ms)
+    out = {"prefill_mixed": {
+        "workload": "mixed-chunked-2048: %d decode rows (ctx U[512,4096]) + %d prompt chunks of %d "
+                    "tokens (cached prefix 512 x U{0..7}), 16q/8kv/128d, bs 256, one paged "
+                    "prefill call" % (nd, len(q_lens) - nd, q_lens[-1]),
+        "gbs": gbs, "tflops": tf, "kernel_ms": round(one_ms, 4),
+        "roofline": {"bound": "hbm" if hbm_bound else "tensor",
+                     "peak": hbm if hbm_bound else tfl, "unit": "GB/s" if hbm_bound else "TFLOP/s",
+                     "frac": frac,
+                     "note": "bytes = each sequence's K/V read once + q and o; the bound is the "
+                             "larger of bytes / HBM peak and causal FLOPs / bf16 peak"},
+        "bytes_per_launch": nbytes, "flops_per_launch": flops,
+        "back_to_back": {"gbs": b_gbs, "tflops": b_tf, "kernel_ms": round(b2b_ms, 4),
+                         "frac": b_frac, "timing": "four calls captured in one CUDA graph, "
+                                                   "replay time / 4"},
+        "as_two_calls": {"ms": round(two_ms, 4),
+                         "timing": "paged_attn_prefill of the chunks, then paged_attn_decode "
+                                   "(+ merge) of the decode rows, four pairs captured in one CUDA "
+                                   "graph, replay time / 4"},
+        "l2": "no flush: the call reads about %d MB of K/V, more than the 129 MB L2" % (nbytes // 10**6),
+    }}
+    del mix, d_ws, c_ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def section_decode_large(args, world, hbm):
     """Large padded decode (GQA group 4, lognormal contexts, padding rows).
     --large-batch / --large-pool scale it down (for profiling captures)."""
@@ -698,6 +777,7 @@ def run_only(args, rank, world):
           "prefill_varlen": lambda: section_prefill_varlen(args, world, hbm, tfl),
           "qk_norm_rope_store": lambda: section_prologue(args, world, hbm),
           "prefill_prefix": lambda: section_prefill_prefix(args, world, hbm, tfl),
+          "prefill_mixed": lambda: section_prefill_mixed(args, world, hbm, tfl),
           "decode_large": lambda: section_decode_large(args, world, hbm)}[args.only]
     return {"metric": METRIC, "only": args.only, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "also": fn()}
@@ -791,6 +871,7 @@ def run_ours(args, rank, world):
     also.update(section_prefill_varlen(args, world, hbm, tfl))
     also.update(section_prologue(args, world, hbm))
     also.update(section_prefill_prefix(args, world, hbm, tfl))
+    also.update(section_prefill_mixed(args, world, hbm, tfl))
     if not args.skip_large:
         also.update(section_decode_large(args, world, hbm))
 
@@ -899,7 +980,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-large", action="store_true")
     ap.add_argument("--only", choices=["decode", "prefill_varlen", "qk_norm_rope_store",
-                                       "prefill_prefix", "decode_large"], default=None,
+                                       "prefill_prefix", "prefill_mixed", "decode_large"],
+                    default=None,
                     help="run one secondary workload alone (for profiling captures)")
     ap.add_argument("--large-batch", type=int, default=256)
     ap.add_argument("--large-pool", type=int, default=40000)

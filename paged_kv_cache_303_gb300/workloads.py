@@ -281,10 +281,29 @@ def large_decode(seed: int = SEED_BASE + 4, batch: int = 256, pads: int = 32,
     return decode_work(heads, ctx, seed, name="large-decode-b256p32")
 
 
+def mixed_chunked(seed: int = SEED_BASE + 5, decode_rows: int = 64, chunks: int = 4,
+                  chunk: int = 496, lo: int = 512, hi: int = 4096, max_prefix_chunks: int = 7,
+                  num_blocks: int = 2048) -> PrefillWork:
+    """A chunked-prefill step with a 2048-token budget, as one paged prefill
+    call: 64 decode rows (one new token each, contexts uniform in [512, 4096]
+    as in the decode workload, so a row's cached prefix is context - 1)
+    followed by 4 prompt chunks of 496 tokens whose prompts already hold
+    512 x U{0..7} tokens in the cache (their earlier chunks)."""
+    g = generator(seed + 1000)
+    ctx = torch.randint(lo, hi + 1, (decode_rows,), generator=g, dtype=torch.int64)
+    pre = torch.randint(0, max_prefix_chunks + 1, (chunks,), generator=g, dtype=torch.int64) * 512
+    q_lens = torch.cat([torch.ones(decode_rows, dtype=torch.int64),
+                        torch.full((chunks,), chunk, dtype=torch.int64)])
+    prefix = torch.cat([ctx - 1, pre])
+    heads = Heads(num_blocks=num_blocks, **QWEN3_HEADS)
+    return prefill_work(heads, q_lens, prefix, seed, name="mixed-chunked-2048")
+
+
 CONFIGS = {
     "tiny": tiny,
     "qwen3-decode-b64": qwen3_decode,
     "varlen-prefill-8x": varlen_prefill,
     "prefix-prefill-16x": prefix_prefill,
     "large-decode-b256p32": large_decode,
+    "mixed-chunked-2048": mixed_chunked,
 }

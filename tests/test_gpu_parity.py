@@ -579,6 +579,16 @@ def test_prefill_unaligned_prefix_full_size():
     _check_lse(lse, ref_lse, "unaligned prefix prefill lse")
 
 
+def test_prefill_mixed_chunked_full_size():
+    """The chunked-prefill mixed batch the benchmark times: 64 decode rows
+    (contexts U[512, 4096]) and 4 chunks of 496 tokens behind cached
+    prefixes of 512 x U{0..7} in one paged call: every output element and
+    every lse against the oracle."""
+    out, lse, ref, ref_lse = _prefix_full_size(W.mixed_chunked(), 821)
+    assert_close(out, ref, "mixed chunked prefill (all rows)")
+    _check_lse(lse, ref_lse, "mixed chunked prefill lse")
+
+
 def test_decode_equals_last_prefill_row_on_gpu():
     """The invariant of the pages (decode step t sees position t) on the CUDA
     path itself: decode over ctx tokens equals the last row of a causal

@@ -6,8 +6,9 @@ head_dim 64 and 128, every power-of-two block size from 1 to 256, length
 mixes that hit the tile edges (0, 1, 63-65, 127-129 rows or keys) beside
 uniform draws, cached prefixes aligned or not to the block size, and decode
 batches with padding rows (context 0), for the decode call and the fused
-store + decode step.  Unused cache slots hold NaN, so a masked key that
-reached a sum would show.  Every case is fixed by its seed.
+store + decode step, and chunked-prefill mixed batches (decode rows among
+prompt chunks in one prefill call).  Unused cache slots hold NaN, so a
+masked key that reached a sum would show.  Every case is fixed by its seed.
 """
 import random
 
@@ -69,6 +70,27 @@ def test_random_paged_prefill(seed):
               for _ in range(n)]
     heads = _heads(rng, bs, [q + p for q, p in zip(q_lens, prefix)])
     _prefill_paged(heads, q_lens, prefix, seed=23000 + seed, growing=rng.random() < 0.3)
+
+
+@pytest.mark.parametrize("seed", range(18))
+def test_random_mixed_prefill(seed):
+    """Chunked-prefill mixed batches: decode rows (one new token behind a
+    cached context) interleaved with prompt chunks (cached prefix or none)
+    in one paged prefill call."""
+    rng = random.Random(29000 + seed)
+    bs = BLOCK_SIZES[seed % len(BLOCK_SIZES)]
+    q_lens, prefix = [], []
+    for _ in range(rng.randint(2, 8)):
+        if rng.random() < 0.5:
+            q_lens.append(1)
+            prefix.append(rng.choice([0, bs - 1, bs, 127, 128]) if rng.random() < 0.3
+                          else rng.randint(1, 2500))
+        else:
+            q_lens.append(_length(rng, 400) or 1)
+            prefix.append(0 if rng.random() < 0.3 else rng.randint(1, 1500))
+    heads = _heads(rng, bs, [q + p for q, p in zip(q_lens, prefix)],
+                   HEAD_SHAPES[seed % len(HEAD_SHAPES)])
+    _prefill_paged(heads, q_lens, prefix, seed=30000 + seed)
 
 
 def _decode_draw(rng: random.Random, seed: int):

@@ -245,6 +245,22 @@ def test_decode_other_block_sizes(bs):
     _decode_case(W.Heads(16, 4, 128, bs, need), ctx, seed=340 + bs)
 
 
+@pytest.mark.parametrize("bs", [512, 1024])
+def test_blocks_larger_than_a_tile(bs):
+    """Block sizes above the 256 of the pages' engine: a block spans several
+    128-key prefill tiles and several decode boxes.  Decode, the fused store +
+    decode step and prefix-cache prefill (prefixes ending inside a block and
+    on a block edge) against the oracle."""
+    from test_gpu_fused import _decode_store_case
+    ctx = [1, bs - 1, bs, bs + 1, 2 * bs + 77, 0]
+    need = sum((c + bs - 1) // bs for c in ctx) + 2
+    _decode_case(W.Heads(16, 8, 128, bs, need), ctx, seed=380 + bs)
+    _decode_store_case(W.Heads(16, 4, 64, bs, need), ctx, seed=381 + bs, cache_seed=382 + bs)
+    q_lens, prefix = [200, 1, 129, 64], [bs, 3, bs + 300, 0]
+    need = sum((q + p + bs - 1) // bs for q, p in zip(q_lens, prefix)) + 2
+    _prefill_paged(W.Heads(16, 8, 128, bs, need), q_lens, prefix, seed=383 + bs)
+
+
 @pytest.mark.parametrize("bs", [1, 2, 4, 8, 128])
 def test_prefill_prefix_cache_other_block_sizes(bs):
     """Block sizes 1, 2 and 4 (shorter than the 8-row swizzle atom: tiles
@@ -587,6 +603,73 @@ def test_prefill_mixed_chunked_full_size():
     out, lse, ref, ref_lse = _prefix_full_size(W.mixed_chunked(), 821)
     assert_close(out, ref, "mixed chunked prefill (all rows)")
     _check_lse(lse, ref_lse, "mixed chunked prefill lse")
+
+
+def test_empty_inputs_are_no_ops():
+    """Zero tokens, zero sequences and a zero batch through every entry point:
+    each call returns without error, writes nothing (the caches keep their
+    canary bits) and leaves no device status."""
+    ops.device_status(clear=True)
+    h = W.Heads(16, 8, 128, 16, 8)
+    kc = W.fill_normal_(torch.empty((8, 16, 8, 128), dtype=torch.bfloat16, device="cuda"), 990)
+    vc = W.fill_normal_(torch.empty_like(kc), 991)
+    k0, v0 = kc.clone(), vc.clone()
+    bt = torch.zeros((0, 4), dtype=torch.int32, device="cuda")
+    none_i = torch.zeros(0, dtype=torch.int32, device="cuda")
+    rows = lambda n, heads: torch.zeros((n, heads, 128), dtype=torch.bfloat16, device="cuda")
+    # slot mapping: no sequences, and sequences with no new tokens
+    assert ops.kv_build_slot_mapping(bt, none_i, dev(torch.zeros(1, dtype=torch.int32)), 16).numel() == 0
+    bt2 = dev(torch.tensor([[0, 1], [2, 3]], dtype=torch.int32))
+    assert ops.kv_build_slot_mapping(bt2, dev(torch.tensor([5, 0], dtype=torch.int32)),
+                                     dev(torch.zeros(3, dtype=torch.int32)), 16).numel() == 0
+    assert ops.kv_build_decode_slots(bt, none_i, 16).numel() == 0
+    ops.kv_store(rows(0, 8), rows(0, 8), kc, vc, none_i)
+    pos = torch.zeros(0, dtype=torch.int64, device="cuda")
+    w = torch.ones(128, dtype=torch.bfloat16, device="cuda")
+    q_out, _ = ops.qk_norm_rope_store(rows(0, 16), rows(0, 8), rows(0, 8), pos, w, w, kc, vc, none_i)
+    assert q_out.shape == (0, 16, 128)
+    assert ops.paged_attn_decode(rows(0, 16), kc, vc, bt, none_i, 1, h.scale).shape == (0, 16, 128)
+    assert ops.paged_attn_decode_store(rows(0, 16), rows(0, 8), rows(0, 8), kc, vc, bt, none_i, 1,
+                                       h.scale).shape == (0, 16, 128)
+    cu0 = dev(torch.zeros(2, dtype=torch.int32))
+    assert ops.paged_attn_prefill(rows(0, 16), rows(0, 8), rows(0, 8), cu0, cu0, 0, 0,
+                                  h.scale).shape == (0, 16, 128)
+    # cached prefixes and no new tokens, through the block tables
+    cuk = dev(torch.tensor([0, 20, 40], dtype=torch.int32))
+    assert ops.paged_attn_prefill(rows(0, 16), None, None, dev(torch.zeros(3, dtype=torch.int32)), cuk,
+                                  0, 20, h.scale, k_cache=kc, v_cache=vc,
+                                  block_tables=bt2).shape == (0, 16, 128)
+    torch.cuda.synchronize()
+    assert torch.equal(kc.view(torch.int16), k0.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), v0.view(torch.int16))
+    assert ops.device_status(clear=True) == 0
+
+
+def test_decode_batch_of_padding_rows_only():
+    """A CUDA-graph batch whose rows are all padding (context 0, table rows of
+    -1): the output is zero, lse is -inf, and the fused step writes nothing."""
+    ops.device_status(clear=True)
+    kc = W.fill_normal_(torch.empty((8, 16, 8, 128), dtype=torch.bfloat16, device="cuda"), 992)
+    vc = W.fill_normal_(torch.empty_like(kc), 993)
+    k0, v0 = kc.clone(), vc.clone()
+    b = 5
+    bt = torch.full((b, 4), -1, dtype=torch.int32, device="cuda")
+    ctx = torch.zeros(b, dtype=torch.int32, device="cuda")
+    q = W.fill_normal_(torch.empty((b, 16, 128), dtype=torch.bfloat16, device="cuda"), 994)
+    kn = W.fill_normal_(torch.empty((b, 8, 128), dtype=torch.bfloat16, device="cuda"), 995)
+    for fused in (False, True):
+        if fused:
+            out, lse = ops.paged_attn_decode_store(q, kn, kn, kc, vc, bt, ctx, 64, 0.125,
+                                                   return_lse=True)
+        else:
+            out, lse = ops.paged_attn_decode(q, kc, vc, bt, ctx, 64, 0.125, return_lse=True)
+        torch.cuda.synchronize()
+        assert torch.equal(out.float(), torch.zeros_like(out.float()))
+        assert bool(torch.isneginf(lse).all())
+    assert torch.equal(ops.kv_build_decode_slots(bt, ctx, 16).cpu(), torch.full((b,), -1, dtype=torch.int32))
+    assert torch.equal(kc.view(torch.int16), k0.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), v0.view(torch.int16))
+    assert ops.device_status(clear=True) == 0
 
 
 def test_decode_equals_last_prefill_row_on_gpu():
